@@ -1,0 +1,42 @@
+/*
+ * wd_bench.h - memory-bandwidth reference kernels for measuring the layer.
+ *
+ * The warp-decode blog (Cursor, "用 warp decode 实现更好的 MoE 模型推理",
+ * section 硬件效率 [Hardware efficiency]) states its layer throughput as a
+ * fraction of the peak a copy kernel reaches with sequential reads.  These
+ * kernels give that denominator on the machine at hand:
+ *   wd_bench_copy  - dst[i] = src[i], 32-byte vectors, grid-stride; bytes moved
+ *                    = 2 * bytes (read + write), the copy-kernel convention;
+ *   wd_bench_read  - streams src once (read only) and folds it into *sink;
+ *   wd_bench_fill  - writes a pattern over buf (used to evict L2 between timed
+ *                    runs when buf is larger than L2).
+ * All pointers are device pointers owned by the caller; src/dst/buf must be
+ * 32-byte aligned and `bytes` a multiple of 32.  Asynchronous on `stream`;
+ * returns 0 on success, else the cudaError_t of the launch.
+ */
+#ifndef WD_BENCH_H_
+#define WD_BENCH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef WD_API
+#define WD_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+WD_API int wd_bench_copy(void* dst, const void* src, size_t bytes, int blocks, void* stream);
+WD_API int wd_bench_read(const void* src, size_t bytes, uint32_t* sink, int blocks, void* stream);
+WD_API int wd_bench_fill(void* buf, size_t bytes, uint32_t value, int blocks, void* stream);
+
+/* Number of streaming multiprocessors of the current device (or -1). */
+WD_API int wd_bench_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WD_BENCH_H_ */

@@ -1,0 +1,141 @@
+/*
+ * wd_moe.h - small-batch MoE decode layer on MXFP8 expert weights ("warp decode").
+ *
+ * The layer (Cursor, "用 warp decode 实现更好的 MoE 模型推理" [Better MoE
+ * inference with warp decode], section 两个 kernel 如何工作 [How the two kernels
+ * work]): for each token b with routed experts e_k = topk_ids[b,k] and routing
+ * weights w_k = topk_w[b,k], k < K,
+ *
+ *     h[b,k,n] = bf16( SiLU(Wg[e_k] x[b])_n * (Wu[e_k] x[b])_n ),   n < I
+ *     y[b,d]   = sum_k w_k * (Wd[e_k] h[b,k,:])_d,                  d < H
+ *     out[b,d] = bf16(y[b,d])
+ *
+ * computed as two kernels organised around outputs rather than experts:
+ *   moe_gate_up_3d_batched - one warp per (token, routed expert, intermediate
+ *                            neuron): streams that neuron's gate and up rows
+ *                            once, dots both against x, writes one BF16 value;
+ *   moe_down_3d_batched    - one warp per (token, output dim): walks all K
+ *                            routed experts' down rows and folds the weighted
+ *                            contributions into one FP32 register accumulator,
+ *                            reduces across the warp with shuffles, writes once.
+ * There is no padding, no gather of activations into expert-major buffers and no
+ * combine pass (section 阶段消除 [Stage elimination], section 消除缓冲区
+ * [Eliminating buffers]).  Activations are BF16, accumulation is FP32 and the
+ * weights are dequantised from MXFP8 as they stream in (section 精度提升
+ * [Accuracy gains]).
+ *
+ * Formats (OCP Microscaling Formats (MX) v1.0):
+ *   weights: E4M3 codes (1 byte) with one E8M0 scale byte (2^(s-127)) per 32
+ *            consecutive elements along the reduction dimension;
+ *   x, h, out: BF16 (IEEE binary32 upper half), round to nearest even on store.
+ *
+ * Memory layout (all row-major, contiguous, device memory, caller-owned):
+ *   x              bf16  [B, H]
+ *   topk_ids       int32 [B, K]
+ *   topk_w         fp32  [B, K]
+ *   gate_up        e4m3  [E, 2I, H]   rows [0, I) = gate, rows [I, 2I) = up
+ *   gate_up_scale  e8m0  [E, 2I, H/32]
+ *   down           e4m3  [E, H, I]
+ *   down_scale     e8m0  [E, H, I/32]
+ *   out            bf16  [B, H]
+ *   workspace      wd_moe_workspace_size(B, K, I) bytes, 256-byte aligned:
+ *                  bytes [0, 4) a 32-bit error flag, bytes [256, ...) the
+ *                  BF16 intermediate h [B, K, I]; a workspace sized for a
+ *                  batch B serves every smaller batch
+ *
+ * Requirements checked on the host (a violation returns an error, nothing is
+ * launched): non-null pointers; B >= 1; 1 <= K <= E; H and I multiples of 32
+ * with H <= 16384 and I <= 16384; K <= 64; B <= 4096; x, gate_up and down
+ * 32-byte aligned; gate_up_scale, down_scale, topk_ids, topk_w, out and
+ * workspace 4-byte aligned (the workspace 256-byte aligned); workspace_bytes
+ * large enough.
+ *
+ * Expert ids are range-checked on the device: an id outside [0, E) contributes
+ * nothing (its h entries are written as 0) and sets the workspace error flag,
+ * which stays set until wd_moe_read_error_flag reads and clears it.  Duplicate
+ * ids within a token are allowed; their contributions add.
+ *
+ * Every entry point that launches work is asynchronous on `stream`: it never
+ * synchronises, never allocates, and returns after the launches.  Launch
+ * failures are reported as WD_ERR_CUDA (cudaGetLastError after the launch).
+ * Calls on different streams must not share a workspace.  `out` must not alias
+ * `x`, the weights or the workspace.
+ */
+#ifndef WD_MOE_H_
+#define WD_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifndef WD_API
+#define WD_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* wd_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum wd_status {
+  WD_OK = 0,
+  WD_ERR_INVALID_ARG = 1,         /* null/misaligned pointer, B/K/E out of range */
+  WD_ERR_UNSUPPORTED_SHAPE = 2,   /* H or I not a multiple of 32, or too large   */
+  WD_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < wd_moe_workspace_size(...) */
+  WD_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed        */
+  WD_ERR_BAD_EXPERT_ID = 5        /* reported by wd_moe_read_error_flag only     */
+} wd_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+WD_API const char* wd_status_string(wd_status s);
+
+/* Bytes of workspace wd_moe_decode needs for (B, K, I): 256 bytes holding the
+ * error flag plus the BF16 intermediate h [B, K, I] rounded up to 256 bytes.
+ * Returns 0 when B, K or I is not positive. */
+WD_API size_t wd_moe_workspace_size(int B, int K, int I);
+
+/* Zero the workspace's error flag (one 4-byte cudaMemsetAsync on `stream`).
+ * Call once after allocating a workspace, before its first use. */
+WD_API wd_status wd_moe_workspace_init(void* workspace, size_t workspace_bytes,
+                                       wd_stream_t stream);
+
+/* The MoE decode layer: both kernels, back to back on `stream` (the second
+ * launched as a programmatic dependent of the first, so that its weight
+ * prefetch overlaps the first kernel's tail).  See the file comment for the
+ * layout and the definition.  h is left in the workspace. */
+WD_API wd_status wd_moe_decode(const void* x, const int32_t* topk_ids, const float* topk_w,
+                        const uint8_t* gate_up, const uint8_t* gate_up_scale,
+                        const uint8_t* down, const uint8_t* down_scale, void* out,
+                        void* workspace, size_t workspace_bytes, int B, int H, int I, int E,
+                        int K, wd_stream_t stream);
+
+/* First kernel alone (moe_gate_up_3d_batched; section 两个 kernel 如何工作,
+ * gate/up paragraph): h [B, K, I] BF16 (caller-owned, 4-byte aligned) from x,
+ * topk_ids and the gate/up weights.  `error_flag` is a device uint32 that is
+ * OR-ed with 1 when an expert id is out of range (may be NULL). */
+WD_API wd_status wd_moe_gate_up(const void* x, const int32_t* topk_ids, const uint8_t* gate_up,
+                         const uint8_t* gate_up_scale, void* h, uint32_t* error_flag, int B,
+                         int H, int I, int E, int K, wd_stream_t stream);
+
+/* Second kernel alone (moe_down_3d_batched; section 两个 kernel 如何工作, down
+ * paragraph): out [B, H] BF16 from h [B, K, I] BF16 (32-byte aligned),
+ * topk_ids, topk_w and the down weights. */
+WD_API wd_status wd_moe_down(const void* h, const int32_t* topk_ids, const float* topk_w,
+                      const uint8_t* down, const uint8_t* down_scale, void* out,
+                      uint32_t* error_flag, int B, int H, int I, int E, int K,
+                      wd_stream_t stream);
+
+/* Copy the workspace's error flag to `*flag` (1 if any call since the last read
+ * saw an expert id outside [0, E), else 0) and clear it.  This call
+ * SYNCHRONISES `stream`.  Returns WD_ERR_BAD_EXPERT_ID when the flag was set. */
+WD_API wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes,
+                                       wd_stream_t stream, int* flag);
+
+/* Number of kernel launches wd_moe_decode issues per call (for accounting). */
+WD_API int wd_moe_launches_per_call(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WD_MOE_H_ */

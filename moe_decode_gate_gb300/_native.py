@@ -1,0 +1,177 @@
+"""ctypes binding of the C-ABI in include/wd_moe.h and include/wd_bench.h.
+
+Argument marshalling only: shapes are read off the tensors, pointers and the
+current CUDA stream are passed through, and a non-OK status raises WdError.
+Every step of the layer runs in the library's CUDA kernels; there is no
+fallback path.  If the library cannot be loaded the import of this module
+fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_LOCK = threading.Lock()
+_LIB = None
+
+WD_OK = 0
+STATUS_NAMES = {0: "WD_OK", 1: "WD_ERR_INVALID_ARG", 2: "WD_ERR_UNSUPPORTED_SHAPE",
+                3: "WD_ERR_WORKSPACE_TOO_SMALL", 4: "WD_ERR_CUDA", 5: "WD_ERR_BAD_EXPERT_ID"}
+
+# (name, restype, argtypes) for every symbol the headers declare
+_P, _I, _SZ, _U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
+SIGNATURES = {
+    "wd_status_string": (ctypes.c_char_p, [_I]),
+    "wd_moe_workspace_size": (_SZ, [_I, _I, _I]),
+    "wd_moe_workspace_init": (_I, [_P, _SZ, _P]),
+    "wd_moe_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_gate_up": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_down": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_read_error_flag": (_I, [_P, _SZ, _P, ctypes.POINTER(_I)]),
+    "wd_moe_launches_per_call": (_I, []),
+    "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
+    "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
+    "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
+    "wd_bench_sm_count": (_I, []),
+}
+
+
+class WdError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.OUT
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwd_moe.so (compiling it first if a source is newer)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.build() if _build.stale() else _build.OUT
+            if not os.path.exists(path):
+                raise RuntimeError(f"native library missing: {path}")
+            handle = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _LIB = handle
+    return _LIB
+
+
+def _check(fn, status):
+    if status != WD_OK:
+        raise WdError(fn, status)
+
+
+def _stream(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dims(x, topk_ids, gate_up):
+    B, H = x.shape
+    K = topk_ids.shape[1]
+    E, I2, H2 = gate_up.shape
+    if H2 != H or topk_ids.shape[0] != B or I2 % 2:
+        raise ValueError("inconsistent shapes")
+    return B, H, I2 // 2, E, K
+
+
+# --------------------------------------------------------------- wd_moe.h ---
+
+def wd_status_string(status: int) -> str:
+    return lib().wd_status_string(status).decode()
+
+
+def wd_moe_workspace_size(B: int, K: int, I: int) -> int:
+    return int(lib().wd_moe_workspace_size(B, K, I))
+
+
+def wd_moe_workspace_init(workspace, stream=None):
+    _check("wd_moe_workspace_init",
+           lib().wd_moe_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+
+
+def wd_moe_decode(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out, workspace,
+                  stream=None):
+    """out[B,H] (bf16) = the MoE decode layer; see include/wd_moe.h."""
+    B, H, I, E, K = _dims(x, topk_ids, gate_up)
+    _check("wd_moe_decode", lib().wd_moe_decode(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(gate_up), _ptr(gate_up_scale), _ptr(down),
+        _ptr(down_scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        B, H, I, E, K, _stream(stream)))
+
+
+def wd_moe_gate_up(x, topk_ids, gate_up, gate_up_scale, h, error_flag=None, stream=None):
+    """h[B,K,I] (bf16) from the first kernel alone."""
+    B, H, I, E, K = _dims(x, topk_ids, gate_up)
+    _check("wd_moe_gate_up", lib().wd_moe_gate_up(
+        _ptr(x), _ptr(topk_ids), _ptr(gate_up), _ptr(gate_up_scale), _ptr(h), _ptr(error_flag),
+        B, H, I, E, K, _stream(stream)))
+
+
+def wd_moe_down(h, topk_ids, topk_w, down, down_scale, out, error_flag=None, stream=None):
+    """out[B,H] (bf16) from the second kernel alone, given h[B,K,I]."""
+    B, K, I = h.shape
+    E, H, I2 = down.shape
+    if I2 != I or topk_ids.shape != (B, K):
+        raise ValueError("inconsistent shapes")
+    _check("wd_moe_down", lib().wd_moe_down(
+        _ptr(h), _ptr(topk_ids), _ptr(topk_w), _ptr(down), _ptr(down_scale), _ptr(out),
+        _ptr(error_flag), B, H, I, E, K, _stream(stream)))
+
+
+def wd_moe_read_error_flag(workspace, stream=None) -> int:
+    """1 if an expert id was out of range since the last read (synchronises)."""
+    flag = ctypes.c_int(0)
+    st = lib().wd_moe_read_error_flag(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream), ctypes.byref(flag))
+    if st not in (WD_OK, 5):
+        raise WdError("wd_moe_read_error_flag", st)
+    return flag.value
+
+
+def wd_moe_launches_per_call() -> int:
+    return int(lib().wd_moe_launches_per_call())
+
+
+# ------------------------------------------------------------- wd_bench.h ---
+
+def wd_bench_copy(dst, src, nbytes=None, blocks=0, stream=None):
+    n = nbytes if nbytes is not None else src.numel() * src.element_size()
+    _check("wd_bench_copy", lib().wd_bench_copy(_ptr(dst), _ptr(src), n, blocks, _stream(stream)))
+
+
+def wd_bench_read(src, sink, nbytes=None, blocks=0, stream=None):
+    n = nbytes if nbytes is not None else src.numel() * src.element_size()
+    _check("wd_bench_read", lib().wd_bench_read(_ptr(src), n, _ptr(sink), blocks, _stream(stream)))
+
+
+def wd_bench_fill(buf, value=0, nbytes=None, blocks=0, stream=None):
+    n = nbytes if nbytes is not None else buf.numel() * buf.element_size()
+    _check("wd_bench_fill", lib().wd_bench_fill(_ptr(buf), n, value, blocks, _stream(stream)))
+
+
+def wd_bench_sm_count() -> int:
+    return int(lib().wd_bench_sm_count())

@@ -1,0 +1,164 @@
+// wd_capi.cu - the C-ABI of the MoE decode layer (declared in include/wd_moe.h).
+//
+// Host-side argument checks, the per-shape launch plan, and the two launches.
+// Nothing here allocates or synchronises except wd_moe_read_error_flag, which
+// is documented to synchronise.
+#include <stdint.h>
+
+#include "../../include/wd_moe.h"
+#include "wd_launch.h"
+
+namespace wd {
+
+// Launch plan.  K1 keeps 2*npw rows of H bytes in flight per warp and does
+// ceil(H/32/32) blocks per lane in passes of cpl; K2 spreads the K*I/32 blocks
+// of the K routed down rows over the lanes in passes of qpl per lane.
+GateUpPlan plan_gate_up(int B, int H, int I, int K) {
+  (void)B;
+  (void)K;
+  const int nblk = H / 32;
+  GateUpPlan p;
+  (void)nblk;
+  p.npw = 2;  // I is a multiple of 32
+  p.cpl = 1;  // H=2048: two passes of 1 KiB per row, 4 rows in flight per warp
+  return p;
+}
+
+DownPlan plan_down(int B, int H, int I, int K) {
+  (void)B;
+  const int nq = K * (I / 32);
+  DownPlan p;
+  p.rpw = 2;  // H is a multiple of 32
+  const int per_lane = (nq + 31) / 32;
+  p.qpl = per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1);
+  return p;
+}
+
+}  // namespace wd
+
+namespace {
+
+constexpr int kMaxB = 4096, kMaxK = 64, kMaxDim = 16384;
+constexpr size_t kFlagBytes = 256;  // the error flag's slot at the start of the workspace
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t h_bytes(int B, int K, int I) {
+  const size_t raw = (size_t)B * K * I * 2;
+  return (raw + 255) / 256 * 256;
+}
+
+wd_status check_dims(int B, int H, int I, int E, int K) {
+  if (B < 1 || B > kMaxB || K < 1 || K > kMaxK || E < 1 || K > E) return WD_ERR_INVALID_ARG;
+  if (H < 32 || I < 32 || H % 32 || I % 32 || H > kMaxDim || I > kMaxDim)
+    return WD_ERR_UNSUPPORTED_SHAPE;
+  return WD_OK;
+}
+
+wd_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? WD_OK : WD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* wd_status_string(wd_status s) {
+  switch (s) {
+    case WD_OK: return "WD_OK";
+    case WD_ERR_INVALID_ARG: return "WD_ERR_INVALID_ARG";
+    case WD_ERR_UNSUPPORTED_SHAPE: return "WD_ERR_UNSUPPORTED_SHAPE";
+    case WD_ERR_WORKSPACE_TOO_SMALL: return "WD_ERR_WORKSPACE_TOO_SMALL";
+    case WD_ERR_CUDA: return "WD_ERR_CUDA";
+    case WD_ERR_BAD_EXPERT_ID: return "WD_ERR_BAD_EXPERT_ID";
+  }
+  return "WD_ERR_UNKNOWN";
+}
+
+size_t wd_moe_workspace_size(int B, int K, int I) {
+  if (B <= 0 || K <= 0 || I <= 0) return 0;
+  return kFlagBytes + h_bytes(B, K, I);
+}
+
+static uint32_t* flag_of(void* workspace) { return static_cast<uint32_t*>(workspace); }
+static void* h_of(void* workspace) { return static_cast<uint8_t*>(workspace) + kFlagBytes; }
+
+wd_status wd_moe_workspace_init(void* workspace, size_t workspace_bytes, wd_stream_t stream) {
+  if (!workspace || !aligned(workspace, 256)) return WD_ERR_INVALID_ARG;
+  if (workspace_bytes < kFlagBytes) return WD_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(cudaMemsetAsync(flag_of(workspace), 0, sizeof(uint32_t),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+wd_status wd_moe_gate_up(const void* x, const int32_t* topk_ids, const uint8_t* gate_up,
+                         const uint8_t* gate_up_scale, void* h, uint32_t* error_flag, int B,
+                         int H, int I, int E, int K, wd_stream_t stream) {
+  wd_status st = check_dims(B, H, I, E, K);
+  if (st != WD_OK) return st;
+  if (!x || !topk_ids || !gate_up || !gate_up_scale || !h) return WD_ERR_INVALID_ARG;
+  if (!aligned(x, 32) || !aligned(gate_up, 32) || !aligned(topk_ids, 4) || !aligned(h, 4) ||
+      (error_flag && !aligned(error_flag, 4)))
+    return WD_ERR_INVALID_ARG;
+  const wd::GateUpArgs a{x, topk_ids, gate_up, gate_up_scale, h, error_flag, B, H, I, E, K};
+  return cuda_status(wd::launch_gate_up(a, wd::plan_gate_up(B, H, I, K),
+                                        reinterpret_cast<cudaStream_t>(stream), true));
+}
+
+wd_status wd_moe_down(const void* h, const int32_t* topk_ids, const float* topk_w,
+                      const uint8_t* down, const uint8_t* down_scale, void* out,
+                      uint32_t* error_flag, int B, int H, int I, int E, int K,
+                      wd_stream_t stream) {
+  wd_status st = check_dims(B, H, I, E, K);
+  if (st != WD_OK) return st;
+  if (!h || !topk_ids || !topk_w || !down || !down_scale || !out) return WD_ERR_INVALID_ARG;
+  if (!aligned(h, 32) || !aligned(down, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
+      !aligned(out, 4) || (error_flag && !aligned(error_flag, 4)))
+    return WD_ERR_INVALID_ARG;
+  const wd::DownArgs a{h, topk_ids, topk_w, down, down_scale, out, error_flag, B, H, I, E, K};
+  return cuda_status(wd::launch_down(a, wd::plan_down(B, H, I, K),
+                                     reinterpret_cast<cudaStream_t>(stream), true));
+}
+
+wd_status wd_moe_decode(const void* x, const int32_t* topk_ids, const float* topk_w,
+                        const uint8_t* gate_up, const uint8_t* gate_up_scale,
+                        const uint8_t* down, const uint8_t* down_scale, void* out,
+                        void* workspace, size_t workspace_bytes, int B, int H, int I, int E,
+                        int K, wd_stream_t stream) {
+  wd_status st = check_dims(B, H, I, E, K);
+  if (st != WD_OK) return st;
+  if (!x || !topk_ids || !topk_w || !gate_up || !gate_up_scale || !down || !down_scale || !out ||
+      !workspace)
+    return WD_ERR_INVALID_ARG;
+  if (!aligned(x, 32) || !aligned(gate_up, 32) || !aligned(down, 32) || !aligned(topk_ids, 4) ||
+      !aligned(topk_w, 4) || !aligned(out, 4) || !aligned(workspace, 256))
+    return WD_ERR_INVALID_ARG;
+  if (workspace_bytes < wd_moe_workspace_size(B, K, I)) return WD_ERR_WORKSPACE_TOO_SMALL;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* flag = flag_of(workspace);
+  void* h = h_of(workspace);
+  const wd::GateUpArgs ga{x, topk_ids, gate_up, gate_up_scale, h, flag, B, H, I, E, K};
+  st = cuda_status(wd::launch_gate_up(ga, wd::plan_gate_up(B, H, I, K), s, true));
+  if (st != WD_OK) return st;
+  const wd::DownArgs da{h, topk_ids, topk_w, down, down_scale, out, flag, B, H, I, E, K};
+  return cuda_status(wd::launch_down(da, wd::plan_down(B, H, I, K), s, true));
+}
+
+wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_stream_t stream,
+                                 int* flag) {
+  if (!workspace || !flag || !aligned(workspace, 256)) return WD_ERR_INVALID_ARG;
+  if (workspace_bytes < kFlagBytes) return WD_ERR_WORKSPACE_TOO_SMALL;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  uint32_t* dflag = flag_of(workspace);
+  cudaError_t e = cudaMemcpyAsync(&v, dflag, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dflag, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return WD_ERR_CUDA;
+  *flag = v ? 1 : 0;
+  return v ? WD_ERR_BAD_EXPERT_ID : WD_OK;
+}
+
+int wd_moe_launches_per_call(void) { return 2; }
+
+}  // extern "C"

@@ -98,10 +98,21 @@ ORACLE_API uint16_t oracle_f64_to_bf16(double v) {
 
 ORACLE_API double oracle_silu(double g) { return g / (1.0 + exp(-g)); }
 
+/* The two decode functions above, tabulated once when the library loads
+ * (each entry is exactly the function's value for that code). */
+static double e4m3_value[256], e8m0_value[256];
+
+__attribute__((constructor)) static void fill_decode_tables(void) {
+  for (int c = 0; c < 256; ++c) {
+    e4m3_value[c] = oracle_e4m3((uint8_t)c);
+    e8m0_value[c] = oracle_e8m0((uint8_t)c);
+  }
+}
+
 /* Dequantised element (row r, column j) of an MXFP8 matrix whose rows hold
  * `cols` codes and cols/32 scales. */
 static double dq(const uint8_t* codes, const uint8_t* scales, long row, int cols, int j) {
-  return oracle_e4m3(codes[row * cols + j]) * oracle_e8m0(scales[row * (cols / 32) + j / 32]);
+  return e4m3_value[codes[row * cols + j]] * e8m0_value[scales[row * (cols / 32) + j / 32]];
 }
 
 /* ------------------------------------------------------------ the layer ---- */

@@ -1,0 +1,128 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the headers
+declare, and rejects bad arguments on the host before any launch.
+
+Every call below fails host validation, so nothing reaches the GPU even on a
+machine that has one.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_decode_gate_gb300 as wd
+from moe_decode_gate_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("wd_moe.h", "wd_bench.h")]
+
+OK, INVALID, SHAPE, SMALL, CUDA, BADID = 0, 1, 2, 3, 4, 5
+
+
+def declared_symbols():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        names += re.findall(r"^WD_API\s+[\w\s\*]+?\b(wd_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_headers_declare_the_expected_entry_points():
+    names = set(declared_symbols())
+    for n in ("wd_moe_decode", "wd_moe_gate_up", "wd_moe_down", "wd_moe_workspace_size",
+              "wd_moe_workspace_init", "wd_moe_read_error_flag", "wd_status_string",
+              "wd_bench_copy", "wd_bench_read", "wd_bench_fill"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = wd.lib()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, name  # and the binding knows its signature
+
+
+def test_library_was_built_for_sm_103a_only():
+    from moe_decode_gate_gb300 import build
+
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+    assert os.path.exists(wd.library_path())
+
+
+def test_status_strings():
+    for code, name in _native.STATUS_NAMES.items():
+        assert wd.wd_status_string(code) == name
+    assert wd.wd_status_string(99) == "WD_ERR_UNKNOWN"
+
+
+def test_workspace_size():
+    # 256-byte flag slot + bf16 h [B, K, I] rounded up to 256 bytes
+    assert wd.wd_moe_workspace_size(1, 8, 768) == 256 + 12288
+    assert wd.wd_moe_workspace_size(32, 8, 768) == 256 + 32 * 8 * 768 * 2
+    assert wd.wd_moe_workspace_size(1, 1, 32) == 256 + 256
+    assert wd.wd_moe_workspace_size(0, 8, 768) == 0
+    assert wd.wd_moe_workspace_size(1, -1, 768) == 0
+
+
+A32 = 0x10000  # a 32-byte-aligned fake address: never dereferenced (validation fails first)
+
+
+def _decode(x=A32, ids=A32, w=A32, gu=A32, gus=A32, dn=A32, dns=A32, out=A32, ws=A32,
+            ws_bytes=1 << 20, B=1, H=2048, I=768, E=128, K=8):
+    return wd.lib().wd_moe_decode(x, ids, w, gu, gus, dn, dns, out, ws, ws_bytes,
+                                  B, H, I, E, K, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), INVALID), (dict(ids=None), INVALID), (dict(w=None), INVALID),
+    (dict(gu=None), INVALID), (dict(gus=None), INVALID), (dict(dn=None), INVALID),
+    (dict(dns=None), INVALID), (dict(out=None), INVALID), (dict(ws=None), INVALID),
+    (dict(B=0), INVALID), (dict(B=4097), INVALID), (dict(K=0), INVALID), (dict(K=65, E=128), INVALID),
+    (dict(K=9, E=8), INVALID), (dict(E=0), INVALID),
+    (dict(H=2047), SHAPE), (dict(H=2064), SHAPE), (dict(I=770), SHAPE), (dict(I=16), SHAPE),
+    (dict(H=16416), SHAPE),
+    (dict(x=A32 + 16), INVALID), (dict(gu=A32 + 16), INVALID), (dict(dn=A32 + 8), INVALID),
+    (dict(ids=A32 + 2), INVALID), (dict(w=A32 + 1), INVALID), (dict(out=A32 + 2), INVALID),
+    (dict(ws=A32 + 128), INVALID),
+    (dict(ws_bytes=256 + 12287), SMALL), (dict(ws_bytes=0), SMALL),
+])
+def test_decode_rejects_bad_arguments_on_the_host(kw, status):
+    assert _decode(**kw) == status
+
+
+def test_split_kernels_reject_bad_arguments():
+    lib = wd.lib()
+    # gate_up: null h, misaligned x, bad shape
+    assert lib.wd_moe_gate_up(A32, A32, A32, A32, None, None, 1, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_gate_up(A32 + 4, A32, A32, A32, A32, None, 1, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_gate_up(A32, A32, A32, A32, A32, None, 1, 2000, 768, 128, 8, None) == SHAPE
+    assert lib.wd_moe_gate_up(A32, A32, A32, A32, A32, A32 + 1, 1, 2048, 768, 128, 8, None) == INVALID
+    # down: h must be 32-byte aligned
+    assert lib.wd_moe_down(A32 + 16, A32, A32, A32, A32, A32, None, 1, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_down(A32, A32, None, A32, A32, A32, None, 1, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_down(A32, A32, A32, A32, A32, A32, None, 1, 2048, 100, 128, 8, None) == SHAPE
+
+
+def test_workspace_calls_reject_bad_arguments():
+    lib = wd.lib()
+    flag = ctypes.c_int(7)
+    assert lib.wd_moe_workspace_init(None, 1 << 20, None) == INVALID
+    assert lib.wd_moe_workspace_init(A32 + 32, 1 << 20, None) == INVALID
+    assert lib.wd_moe_workspace_init(A32, 16, None) == SMALL
+    assert lib.wd_moe_read_error_flag(A32, 1 << 20, None, None) == INVALID
+    assert lib.wd_moe_read_error_flag(A32 + 64, 1 << 20, None, ctypes.byref(flag)) == INVALID
+    assert lib.wd_moe_read_error_flag(A32, 8, None, ctypes.byref(flag)) == SMALL
+    assert flag.value == 7  # untouched on error
+
+
+def test_bench_kernels_reject_unaligned_buffers():
+    lib = wd.lib()
+    einval = 1  # cudaErrorInvalidValue
+    assert lib.wd_bench_copy(A32, A32 + 16, 1024, 0, None) == einval
+    assert lib.wd_bench_copy(A32, A32, 1000, 0, None) == einval
+    assert lib.wd_bench_read(A32, 1024, None, 0, None) == einval
+    assert lib.wd_bench_fill(None, 1024, 0, 0, None) == einval
+
+
+def test_launch_count():
+    assert wd.wd_moe_launches_per_call() == 2

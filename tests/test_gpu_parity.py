@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA kernels through the C-ABI against the CPU oracle.
+
+Every case compares element by element with the tolerance in tests/parity.py,
+on seeded synthetic inputs (synth/), at sizes that span several CTAs and leave
+ragged tails, and on the Qwen-3-style layer (H=2048, I=768, E=128, K=8) at
+B = 1..32 with the routing patterns of the benchmark.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import moe_decode_gate_gb300 as wd
+
+from parity import compare, from_dev_bf16, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+_WEIGHTS = {}
+
+
+def weights(wl, layer=0):
+    key = (wl.seed, layer, wl.H, wl.I, wl.E)
+    if key not in _WEIGHTS:
+        gu, gus = synth.gate_up(wl.seed, layer, wl.E, wl.H, wl.I)
+        dn, dns = synth.down(wl.seed, layer, wl.E, wl.H, wl.I)
+        _WEIGHTS.clear()  # keep one full layer in host memory at a time
+        _WEIGHTS[key] = (gu, gus, dn, dns)
+    return _WEIGHTS[key]
+
+
+def inputs(wl, B, layer=0):
+    xs = synth.x(wl.seed, layer, B, wl.H)
+    ids, w = synth.route(wl.seed, layer, B, wl.E, wl.K, mode=wl.route)
+    return xs, ids, w
+
+
+def run_layer(dev, xs, ids, w, gu, gus, dn, dns, stream=None):
+    B, K = ids.shape
+    I = gu.shape[1] // 2
+    layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=K, max_batch=B, device=dev)
+    out = torch.empty((B, gu.shape[2]), dtype=torch.bfloat16, device=dev)
+    layer(to_dev_bf16(xs, dev), to_dev(ids, dev), to_dev(w, dev), out=out, stream=stream)
+    torch.cuda.synchronize(dev)
+    h = layer.workspace[256:256 + B * K * I * 2].view(torch.int16).view(B, K, I)
+    flag = wd.wd_moe_read_error_flag(layer.workspace)
+    return from_dev_bf16(out), h.cpu().numpy().view(np.uint16), flag
+
+
+def check_layer(dev, xs, ids, w, gu, gus, dn, dns, what):
+    I, E = gu.shape[1] // 2, gu.shape[0]
+    want, want_h, _, bad = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, I, E, with_f64=True)
+    got, got_h, flag = run_layer(dev, xs, ids, w, gu, gus, dn, dns)
+    compare(got_h.reshape(-1, I), want_h.reshape(-1, I), what + " h")
+    stats = compare(got, want, what + " out")
+    assert flag == (1 if bad else 0)
+    return stats
+
+
+def test_tiny_layer(cuda_device):
+    wl = synth.WORKLOADS["tiny"]
+    s = check_layer(cuda_device, *inputs(wl, 1), *weights(wl), "tiny")
+    assert s["frac_equal"] > 0.9
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16, 32])
+def test_qwen3_layer_batch_sweep(cuda_device, B):
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    s = check_layer(cuda_device, *inputs(wl, B), *weights(wl), f"sweep B={B}")
+    assert s["frac_equal"] > 0.9
+
+
+@pytest.mark.parametrize("name", ["qwen3_zipf", "qwen3_fixed", "qwen3_disjoint"])
+def test_qwen3_routing_stress_b32(cuda_device, name):
+    wl = synth.WORKLOADS[name]
+    check_layer(cuda_device, *inputs(wl, 32), *weights(wl), name)
+
+
+def test_gate_up_kernel_alone(cuda_device):
+    wl = synth.WORKLOADS["qwen3_b1"]
+    gu, gus, _, _ = weights(wl)
+    for B in (1, 3):
+        xs, ids, _ = inputs(wl, B)
+        want = oracle.gate_up(xs, ids, gu, gus, wl.I, wl.E)
+        h = torch.empty((B, wl.K, wl.I), dtype=torch.bfloat16, device=cuda_device)
+        flag = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+        wd.wd_moe_gate_up(to_dev_bf16(xs, cuda_device), to_dev(ids, cuda_device),
+                          to_dev(gu, cuda_device), to_dev(gus, cuda_device), h, error_flag=flag)
+        torch.cuda.synchronize()
+        compare(from_dev_bf16(h).reshape(-1, wl.I), want.reshape(-1, wl.I), f"gate_up B={B}")
+        assert int(flag.item()) == 0
+
+
+def test_down_kernel_alone_on_oracle_h(cuda_device):
+    """The second kernel gets the ORACLE's h, so its parity does not depend on the first."""
+    wl = synth.WORKLOADS["qwen3_b1"]
+    gu, gus, dn, dns = weights(wl)
+    B = 4
+    xs, ids, w = inputs(wl, B)
+    h = oracle.gate_up(xs, ids, gu, gus, wl.I, wl.E)
+    want = oracle.down(h, ids, w, dn, dns, wl.H, wl.E)
+    out = torch.empty((B, wl.H), dtype=torch.bfloat16, device=cuda_device)
+    wd.wd_moe_down(to_dev_bf16(h, cuda_device), to_dev(ids, cuda_device), to_dev(w, cuda_device),
+                   to_dev(dn, cuda_device), to_dev(dns, cuda_device), out)
+    torch.cuda.synchronize()
+    compare(from_dev_bf16(out), want, "down")
+
+
+def _random_case(seed, B, H, I, E, K, route="uniform"):
+    wl = synth.Workload(f"ragged{seed}", seed, H, I, E, K, (B,), route=route)
+    gu, gus = synth.gate_up(seed, 0, E, H, I)
+    dn, dns = synth.down(seed, 0, E, H, I)
+    return inputs(wl, B) + (gu, gus, dn, dns)
+
+
+@pytest.mark.parametrize("B,H,I,E,K", [
+    (1, 32, 32, 1, 1),        # smallest legal layer: one block per row
+    (3, 288, 96, 5, 3),       # 9 and 3 blocks per row: most lanes idle, ragged
+    (5, 1056, 160, 7, 2),     # 33 blocks per gate row: one lane gets two
+    (2, 4096, 256, 4, 4),     # 128 blocks per gate row: four passes per lane
+    (7, 2048, 2048, 6, 6),    # K2 virtual stream of 384 blocks: several passes
+    (33, 512, 768, 16, 8),    # odd batch above 32
+    (64, 2048, 768, 128, 8),  # batch 64 on the full-size layer
+    (2, 128, 64, 3, 3),       # K == E: every expert routed
+])
+def test_ragged_and_edge_shapes(cuda_device, B, H, I, E, K):
+    case = _random_case(100 + B + H + I, B, H, I, E, K)
+    check_layer(cuda_device, *case, f"B={B} H={H} I={I} E={E} K={K}")
+
+
+def test_bad_expert_ids_are_skipped_and_flagged(cuda_device):
+    xs, ids, w, gu, gus, dn, dns = _random_case(7, 4, 256, 128, 8, 3)
+    ids = ids.copy()
+    ids[0, 1], ids[2, 0], ids[3, 2] = -1, 8, 1 << 30
+    want, want_h, _, bad = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, 128, 8, with_f64=True)
+    assert bad == 3
+    got, got_h, flag = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns)
+    assert flag == 1
+    assert not got_h[0, 1].any() and not got_h[2, 0].any()
+    compare(got, want, "bad ids")
+
+
+def test_error_flag_clears_after_read(cuda_device):
+    xs, ids, w, gu, gus, dn, dns = _random_case(8, 2, 256, 128, 8, 2)
+    bad_ids = ids.copy()
+    bad_ids[1, 1] = -5
+    layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=2, max_batch=2, device=cuda_device)
+    x_d = to_dev_bf16(xs, cuda_device)
+    w_d = to_dev(w, cuda_device)
+    layer(x_d, to_dev(bad_ids, cuda_device), w_d)
+    assert wd.wd_moe_read_error_flag(layer.workspace) == 1
+    layer(x_d, to_dev(ids, cuda_device), w_d)
+    assert wd.wd_moe_read_error_flag(layer.workspace) == 0
+
+
+def test_duplicate_ids_and_zero_weights(cuda_device):
+    xs, ids, w, gu, gus, dn, dns = _random_case(9, 6, 512, 256, 8, 4)
+    ids = ids.copy()
+    w = w.copy()
+    ids[0, :] = 3           # one expert four times
+    ids[1, 1] = ids[1, 0]   # a duplicate pair
+    w[2, :] = 0.0           # a token with all-zero routing weights
+    w[3, 1] = 0.0
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, "duplicates / zero weights")
+
+
+def test_extreme_block_scales(cuda_device):
+    """Scales far from 1 (2^-40 .. 2^+20) and subnormal E4M3 codes in every block."""
+    xs, ids, w, gu, gus, dn, dns = _random_case(10, 3, 512, 128, 6, 3)
+    rng = np.random.default_rng(0)
+    gus = (127 + rng.integers(-40, 8, gus.shape)).astype(np.uint8)
+    dns = (127 + rng.integers(-20, 20, dns.shape)).astype(np.uint8)
+    gu = gu.copy()
+    gu[..., ::32] = rng.integers(1, 8, gu[..., ::32].shape)  # subnormal codes
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, "extreme scales")
+
+
+def test_deterministic_and_stream_ordered(cuda_device):
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    xs, ids, w = inputs(wl, 8)
+    gu, gus, dn, dns = weights(wl)
+    s = torch.cuda.Stream(device=cuda_device)
+    with torch.cuda.stream(s):
+        a, _, _ = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, stream=s)
+    b, _, _ = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns)
+    assert np.array_equal(a, b)  # no atomics in any reduction: bit-identical reruns
+
+
+def test_captured_in_a_cuda_graph(cuda_device):
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    xs, ids, w = inputs(wl, 4)
+    gu, gus, dn, dns = weights(wl)
+    layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=wl.K, max_batch=4, device=cuda_device)
+    x_d, ids_d, w_d = to_dev_bf16(xs, cuda_device), to_dev(ids, cuda_device), to_dev(w, cuda_device)
+    out = torch.empty((4, wl.H), dtype=torch.bfloat16, device=cuda_device)
+    s = torch.cuda.Stream(device=cuda_device)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer(x_d, ids_d, w_d, out=out)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    want = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, wl.I, wl.E)
+    compare(from_dev_bf16(out), want, "graph replay")
+
+
+def test_smaller_batch_reuses_a_larger_workspace(cuda_device):
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    gu, gus, dn, dns = weights(wl)
+    layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=wl.K, max_batch=32, device=cuda_device)
+    for B in (32, 3):
+        xs, ids, w = inputs(wl, B)
+        out = layer(to_dev_bf16(xs, cuda_device), to_dev(ids, cuda_device), to_dev(w, cuda_device))
+        torch.cuda.synchronize()
+        want = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, wl.I, wl.E)
+        compare(from_dev_bf16(out), want, f"shared workspace B={B}")
+    assert wd.wd_moe_read_error_flag(layer.workspace) == 0
