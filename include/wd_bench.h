@@ -35,6 +35,10 @@ WD_API int wd_bench_fill(void* buf, size_t bytes, uint32_t value, int blocks, vo
 /* Number of streaming multiprocessors of the current device (or -1). */
 WD_API int wd_bench_sm_count(void);
 
+/* Spec DRAM bandwidth of the current device in GB/s: 2 (double data rate)
+ * x peak memory clock x bus width / 8, from the device attributes; -1 on error. */
+WD_API double wd_bench_spec_gbs(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,7 @@ from ._native import (  # noqa: F401
     wd_bench_fill,
     wd_bench_read,
     wd_bench_sm_count,
+    wd_bench_spec_gbs,
     wd_moe_decode,
     wd_moe_down,
     wd_moe_gate_up,

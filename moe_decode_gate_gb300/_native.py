@@ -36,6 +36,7 @@ SIGNATURES = {
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
     "wd_bench_sm_count": (_I, []),
+    "wd_bench_spec_gbs": (ctypes.c_double, []),
 }
 
 
@@ -175,3 +176,7 @@ def wd_bench_fill(buf, value=0, nbytes=None, blocks=0, stream=None):
 
 def wd_bench_sm_count() -> int:
     return int(lib().wd_bench_sm_count())
+
+
+def wd_bench_spec_gbs() -> float:
+    return float(lib().wd_bench_spec_gbs())

@@ -70,6 +70,14 @@ int wd_bench_sm_count(void) {
   return sms;
 }
 
+double wd_bench_spec_gbs(void) {
+  int dev = 0, khz = 0, bits = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1.0;
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrMemoryClockRate, dev) != cudaSuccess) return -1.0;
+  if (cudaDeviceGetAttribute(&bits, cudaDevAttrGlobalMemoryBusWidth, dev) != cudaSuccess) return -1.0;
+  return 2.0 * khz * 1e3 * (bits / 8.0) / 1e9;
+}
+
 int wd_bench_copy(void* dst, const void* src, size_t bytes, int blocks, void* stream) {
   if (!ok32(dst, bytes) || !ok32(src, bytes)) return (int)cudaErrorInvalidValue;
   copy_kernel<<<blocks_or_default(blocks), 256, 0, (cudaStream_t)stream>>>(
