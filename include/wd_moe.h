@@ -134,6 +134,33 @@ WD_API wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes,
 /* Number of kernel launches wd_moe_decode issues per call (for accounting). */
 WD_API int wd_moe_launches_per_call(void);
 
+/* The same layer as wd_moe_decode, for callers that cannot allocate device
+ * memory and so cannot provide a workspace: for example a plugin whose host
+ * framework owns all device memory and forbids allocating while it runs, or a
+ * latency-critical caller that cannot pay for cudaMalloc's possible implicit
+ * device synchronisation.  The blog has no counterpart: this is a property of
+ * this library's interface, not of the method.
+ *
+ * The intermediate h lives in a 1 MiB array compiled into the library
+ * (file-scope device memory that every GPU loading the library holds until the
+ * process exits), so B * K * I * 2 must be at most 1048576 bytes (B <= 85 at
+ * K = 8, I = 768); larger sizes return WD_ERR_WORKSPACE_TOO_SMALL before any
+ * launch.  The function allocates nothing and calls no allocating routine.
+ *
+ * The first call made with a given device current looks up that device's
+ * address of the array (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the one array: calls that can overlap on the
+ * GPU (for instance on two streams with no ordering between them) race on it
+ * and must not be issued.  Nothing in the array needs clearing, since each call
+ * writes every h element it later reads.  Out-of-range expert ids contribute
+ * nothing, as in wd_moe_decode, but are not reported (no error flag is kept).
+ * Arguments, layouts and the other checks are those of wd_moe_decode. */
+WD_API wd_status wd_moe_decode_no_alloc(const void* x, const int32_t* topk_ids,
+                                        const float* topk_w, const uint8_t* gate_up,
+                                        const uint8_t* gate_up_scale, const uint8_t* down,
+                                        const uint8_t* down_scale, void* out, int B, int H, int I,
+                                        int E, int K, wd_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

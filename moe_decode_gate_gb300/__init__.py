@@ -20,6 +20,7 @@ from ._native import (  # noqa: F401
     wd_bench_sm_count,
     wd_bench_spec_gbs,
     wd_moe_decode,
+    wd_moe_decode_no_alloc,
     wd_moe_down,
     wd_moe_gate_up,
     wd_moe_launches_per_call,

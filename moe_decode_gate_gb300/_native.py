@@ -32,6 +32,7 @@ SIGNATURES = {
     "wd_moe_down": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_moe_read_error_flag": (_I, [_P, _SZ, _P, ctypes.POINTER(_I)]),
     "wd_moe_launches_per_call": (_I, []),
+    "wd_moe_decode_no_alloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
@@ -155,6 +156,17 @@ def wd_moe_read_error_flag(workspace, stream=None) -> int:
 
 def wd_moe_launches_per_call() -> int:
     return int(lib().wd_moe_launches_per_call())
+
+
+def wd_moe_decode_no_alloc(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out,
+                           stream=None):
+    """The layer without a workspace, for callers that cannot allocate device
+    memory: h lives in a 1 MiB array inside the library (B*K*I*2 <= 1 MiB).
+    Calls that may overlap on the GPU share that array and must not be issued."""
+    B, H, I, E, K = _dims(x, topk_ids, gate_up)
+    _check("wd_moe_decode_no_alloc", lib().wd_moe_decode_no_alloc(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(gate_up), _ptr(gate_up_scale), _ptr(down),
+        _ptr(down_scale), _ptr(out), B, H, I, E, K, _stream(stream)))
 
 
 # ------------------------------------------------------------- wd_bench.h ---
