@@ -72,7 +72,9 @@ def read_peaks_file():
 
 def kernel_sources_sha():
     h = hashlib.sha256()
-    for f in ("wd_gate_up.cu", "wd_down.cu", "wd_device.cuh", "wd_capi.cu"):
+    for f in sorted(os.listdir(os.path.join(ROOT, "moe_decode_gate_gb300", "csrc"))):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(os.path.join(ROOT, "moe_decode_gate_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

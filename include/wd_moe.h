@@ -134,6 +134,19 @@ WD_API wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes,
 /* Number of kernel launches wd_moe_decode issues per call (for accounting). */
 WD_API int wd_moe_launches_per_call(void);
 
+/* Override the per-shape launch plan (tuning and tests; not needed in normal
+ * use).  `spec` is a comma-separated list of
+ *   "gu=batched:<neurons per warp>:<blocks per lane per pass>"
+ *   "gu=rowshare:<neurons per warp>:<words per step>"   (tokens share rows)
+ *   "dn=<output dims per warp>:<blocks per lane per pass>"
+ *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel>"
+ * NULL or "" restores the built-in plan.  Returns WD_ERR_INVALID_ARG for an
+ * unparsable spec (the plan is then unchanged); an unsupported combination
+ * makes later launches fail with WD_ERR_CUDA.  Process-wide; do not call while
+ * another thread is inside a wd_moe_* call.  The WD_PLAN environment variable,
+ * read at the first launch, sets the initial override. */
+WD_API wd_status wd_moe_set_plan(const char* spec);
+
 /* The same layer as wd_moe_decode, for callers that cannot allocate device
  * memory and so cannot provide a workspace: for example a plugin whose host
  * framework owns all device memory and forbids allocating while it runs, or a

@@ -25,6 +25,7 @@ from ._native import (  # noqa: F401
     wd_moe_gate_up,
     wd_moe_launches_per_call,
     wd_moe_read_error_flag,
+    wd_moe_set_plan,
     wd_moe_workspace_init,
     wd_moe_workspace_size,
     wd_status_string,

@@ -33,6 +33,7 @@ SIGNATURES = {
     "wd_moe_read_error_flag": (_I, [_P, _SZ, _P, ctypes.POINTER(_I)]),
     "wd_moe_launches_per_call": (_I, []),
     "wd_moe_decode_no_alloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_set_plan": (_I, [ctypes.c_char_p]),
     "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
@@ -156,6 +157,11 @@ def wd_moe_read_error_flag(workspace, stream=None) -> int:
 
 def wd_moe_launches_per_call() -> int:
     return int(lib().wd_moe_launches_per_call())
+
+
+def wd_moe_set_plan(spec=None):
+    """Override the launch plan (see include/wd_moe.h); None restores the default."""
+    _check("wd_moe_set_plan", lib().wd_moe_set_plan(None if spec is None else spec.encode()))
 
 
 def wd_moe_decode_no_alloc(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out,

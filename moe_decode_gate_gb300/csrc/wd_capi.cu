@@ -4,33 +4,124 @@
 // Nothing here allocates or synchronises except wd_moe_read_error_flag, which
 // is documented to synchronise.
 #include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "../../include/wd_moe.h"
 #include "wd_launch.h"
 
 namespace wd {
 
-// Launch plan.  K1 keeps 2*npw rows of H bytes in flight per warp and does
-// ceil(H/32/32) blocks per lane in passes of cpl; K2 spreads the K*I/32 blocks
-// of the K routed down rows over the lanes in passes of qpl per lane.
-GateUpPlan plan_gate_up(int B, int H, int I, int K) {
-  (void)B;
-  (void)K;
-  const int nblk = H / 32;
-  GateUpPlan p;
-  (void)nblk;
-  p.npw = 2;  // I is a multiple of 32
-  p.cpl = 1;  // H=2048: two passes of 1 KiB per row, 4 rows in flight per warp
+// Launch plan.  The batched gate/up kernel keeps 2*npw rows of H bytes in
+// flight per warp and does ceil(H/32/32) blocks per lane in passes of cpl; the
+// shared-row variant serves every token of an expert from one dequantised row
+// and is used once tokens start to share experts.  The down kernel spreads the
+// K*I/32 blocks of the K routed rows over the lanes in passes of qpl per lane.
+//
+// wd_moe_set_plan (or the WD_PLAN environment variable, read at the first
+// call) overrides the choice for tuning sweeps and tests:
+//   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>",
+//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>",
+//   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
+namespace {
+
+struct PlanOverride {
+  int gu_variant = -1, gu_npw = 0, gu_cpl = 0;
+  int dn_variant = -1, dn_rpw = 0, dn_qpl = 0;
+  int rowshare_min_b = 16;
+};
+
+bool parse_plan(const char* spec, PlanOverride* out) {
+  PlanOverride p;
+  if (spec && *spec) {
+    char buf[256];
+    strncpy(buf, spec, sizeof(buf) - 1);
+    buf[sizeof(buf) - 1] = 0;
+    char* save = nullptr;
+    for (char* tok = strtok_r(buf, ",", &save); tok; tok = strtok_r(nullptr, ",", &save)) {
+      int a = 0, b = 0;
+      if (sscanf(tok, "gu=batched:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpBatched;
+        p.gu_npw = a;
+        p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=stream:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpStream;
+        p.gu_npw = a;
+        p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=rowshare:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpRowShare;
+        p.gu_npw = a;
+        p.gu_cpl = b;
+      } else if (sscanf(tok, "dn=stream:%d", &a) == 1) {
+        p.dn_variant = kDownStream;
+        p.dn_qpl = a;
+      } else if (sscanf(tok, "dn=%d:%d", &a, &b) == 2) {
+        p.dn_variant = kDownBatched;
+        p.dn_rpw = a;
+        p.dn_qpl = b;
+      } else if (sscanf(tok, "rowshare_min_b=%d", &a) == 1) {
+        p.rowshare_min_b = a;
+      } else {
+        return false;
+      }
+    }
+  }
+  *out = p;
+  return true;
+}
+
+PlanOverride& plan_override() {
+  static PlanOverride o = [] {
+    PlanOverride p;
+    parse_plan(getenv("WD_PLAN"), &p);
+    return p;
+  }();
+  return o;
+}
+
+}  // namespace
+
+GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
+  const PlanOverride& o = plan_override();
+  const bool rowshare_ok = B * K <= kRowShareMaxSlots && E <= kRowShareMaxExperts;
+  if (o.gu_variant == kGateUpStream && gate_up_stream_supported(B, H, I, E, K, o.gu_npw))
+    return {kGateUpStream, o.gu_npw, o.gu_cpl};
+  if (o.gu_variant == kGateUpRowShare && rowshare_ok) return {kGateUpRowShare, o.gu_npw, o.gu_cpl};
+  if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
+  // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack: one
+  // warp per (token, slot, neuron pair) while tokens rarely share experts; one
+  // dequantised row per expert for all its tokens once they do
+  if (rowshare_ok && B >= o.rowshare_min_b) return {kGateUpRowShare, 2, 2};
+  return {kGateUpBatched, 2, 1};  // two passes of 1 KiB per row at H=2048, 4 rows in flight
+}
+
+DownPlan plan_down(int B, int H, int I, int K, int E) {
+  const PlanOverride& o = plan_override();
+  if (o.dn_variant == kDownStream && down_stream_supported(B, H, I, E, K))
+    return DownPlan{0, o.dn_qpl, kDownStream};
+  if (o.dn_variant == kDownBatched) return DownPlan{o.dn_rpw, o.dn_qpl, kDownBatched};
+  if (B >= 8) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
+  const int nq = K * (I / 32);
+  const int per_lane = (nq + 31) / 32;
+  return DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
+  GateUpPlan p = plan_gate_up(a.B, a.H, a.I, a.K, a.E);
+  if (p.variant == kGateUpStream && !(aligned16(a.gate_up) && aligned16(a.gate_up_scale)))
+    p = {kGateUpBatched, 2, 1};
   return p;
 }
 
-DownPlan plan_down(int B, int H, int I, int K) {
-  (void)B;
-  const int nq = K * (I / 32);
-  DownPlan p;
-  p.rpw = 2;  // H is a multiple of 32
-  const int per_lane = (nq + 31) / 32;
-  p.qpl = per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1);
+DownPlan plan_down_for(const DownArgs& a) {
+  DownPlan p = plan_down(a.B, a.H, a.I, a.K, a.E);
+  if (p.variant == kDownStream && !(aligned16(a.down) && aligned16(a.down_scale))) {
+    const int per_lane = (a.K * (a.I / 32) + 31) / 32;
+    p = DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
+  }
   return p;
 }
 
@@ -101,7 +192,7 @@ wd_status wd_moe_gate_up(const void* x, const int32_t* topk_ids, const uint8_t* 
       (error_flag && !aligned(error_flag, 4)))
     return WD_ERR_INVALID_ARG;
   const wd::GateUpArgs a{x, topk_ids, gate_up, gate_up_scale, h, error_flag, B, H, I, E, K};
-  return cuda_status(wd::launch_gate_up(a, wd::plan_gate_up(B, H, I, K),
+  return cuda_status(wd::launch_gate_up(a, wd::plan_gate_up_for(a),
                                         reinterpret_cast<cudaStream_t>(stream), true));
 }
 
@@ -116,8 +207,10 @@ wd_status wd_moe_down(const void* h, const int32_t* topk_ids, const float* topk_
       !aligned(out, 4) || (error_flag && !aligned(error_flag, 4)))
     return WD_ERR_INVALID_ARG;
   const wd::DownArgs a{h, topk_ids, topk_w, down, down_scale, out, error_flag, B, H, I, E, K};
-  return cuda_status(wd::launch_down(a, wd::plan_down(B, H, I, K),
-                                     reinterpret_cast<cudaStream_t>(stream), true));
+  // launched without programmatic dependent launch: the kernel may read the
+  // routing before waiting on its predecessor, which here can be anything
+  return cuda_status(wd::launch_down(a, wd::plan_down_for(a),
+                                     reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 wd_status wd_moe_decode(const void* x, const int32_t* topk_ids, const float* topk_w,
@@ -138,10 +231,10 @@ wd_status wd_moe_decode(const void* x, const int32_t* topk_ids, const float* top
   uint32_t* flag = flag_of(workspace);
   void* h = h_of(workspace);
   const wd::GateUpArgs ga{x, topk_ids, gate_up, gate_up_scale, h, flag, B, H, I, E, K};
-  st = cuda_status(wd::launch_gate_up(ga, wd::plan_gate_up(B, H, I, K), s, true));
+  st = cuda_status(wd::launch_gate_up(ga, wd::plan_gate_up_for(ga), s, true));
   if (st != WD_OK) return st;
   const wd::DownArgs da{h, topk_ids, topk_w, down, down_scale, out, flag, B, H, I, E, K};
-  return cuda_status(wd::launch_down(da, wd::plan_down(B, H, I, K), s, true));
+  return cuda_status(wd::launch_down(da, wd::plan_down_for(da), s, true));
 }
 
 wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_stream_t stream,
@@ -160,5 +253,12 @@ wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_str
 }
 
 int wd_moe_launches_per_call(void) { return 2; }
+
+wd_status wd_moe_set_plan(const char* spec) {
+  wd::PlanOverride p;
+  if (!wd::parse_plan(spec, &p)) return WD_ERR_INVALID_ARG;
+  wd::plan_override() = p;
+  return WD_OK;
+}
 
 }  // extern "C"

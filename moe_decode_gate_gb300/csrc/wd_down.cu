@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(256, 2) moe_down_3d_batched(
     const __nv_bfloat16* __restrict__ h, const int32_t* __restrict__ topk_ids,
     const float* __restrict__ topk_w, const uint8_t* __restrict__ down,
     const uint8_t* __restrict__ down_scale, __nv_bfloat16* __restrict__ out,
-    uint32_t* __restrict__ error_flag, int B, int H, int I, int E, int K) {
+    uint32_t* __restrict__ error_flag, int B, int H, int I, int E, int K,
+    unsigned long long ib_magic) {
   grid_launch_dependents();
 
   const int lane = threadIdx.x & 31;
@@ -63,7 +64,9 @@ __global__ void __launch_bounds__(256, 2) moe_down_3d_batched(
       const int q = q0 + lane + 32 * j;
       ok[j] = false;
       if (q < nq) {
-        const int k = q / ib;
+        // k = q / ib without a division: ib_magic = ceil(2^32 / ib) is exact for
+        // q * ib < 2^32 (q < K*ib <= 32768, ib <= 512)
+        const int k = (int)(((unsigned long long)q * ib_magic) >> 32);
         const int blk = q - k * ib;
         const int e = __ldg(ids + k);
         if (e >= 0 && e < E) {
@@ -110,6 +113,8 @@ template <int RPW, int QPL>
 static cudaError_t launch_down_t(const DownArgs& a, cudaStream_t stream, bool pdl) {
   const long long warps = (long long)(a.H / RPW) * a.B;
   const long long blocks = (warps + 7) / 8;
+  const unsigned long long ib = (unsigned long long)(a.I / 32);
+  const unsigned long long ib_magic = ((1ull << 32) + ib - 1) / ib;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(256);
@@ -122,10 +127,11 @@ static cudaError_t launch_down_t(const DownArgs& a, cudaStream_t stream, bool pd
   return cudaLaunchKernelEx(&cfg, moe_down_3d_batched<RPW, QPL>,
                             reinterpret_cast<const __nv_bfloat16*>(a.h), a.topk_ids, a.topk_w,
                             a.down, a.down_scale, reinterpret_cast<__nv_bfloat16*>(a.out),
-                            a.error_flag, a.B, a.H, a.I, a.E, a.K);
+                            a.error_flag, a.B, a.H, a.I, a.E, a.K, ib_magic);
 }
 
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl) {
+  if (p.variant == kDownStream) return launch_down_stream(a, p, stream, pdl);
 #define WD_DN_CASE(RPW, QPL) \
   if (p.rpw == RPW && p.qpl == QPL) return launch_down_t<RPW, QPL>(a, stream, pdl);
   WD_DN_CASE(1, 1)
@@ -135,6 +141,8 @@ cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t strea
   WD_DN_CASE(2, 1)
   WD_DN_CASE(2, 2)
   WD_DN_CASE(2, 3)
+  WD_DN_CASE(4, 1)
+  WD_DN_CASE(4, 2)
 #undef WD_DN_CASE
   return cudaErrorInvalidConfiguration;
 }

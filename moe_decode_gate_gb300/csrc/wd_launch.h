@@ -27,20 +27,50 @@ struct DownArgs {
   int B, H, I, E, K;
 };
 
+// Limits of the shared-row gate/up variant (shared-memory routing tables).
+constexpr int kRowShareMaxSlots = 2048;    // B * K
+constexpr int kRowShareMaxExperts = 4096;  // E
+// Limit of the streamed variants' per-CTA routing tables (B * K).
+constexpr int kStreamMaxSlots = 256;
+
+enum GateUpVariant {
+  kGateUpBatched = 0,   // moe_gate_up_3d_batched: one warp per (token, slot, neuron group)
+  kGateUpRowShare = 1,  // moe_gate_up_rowshare: one warp per (expert, neuron group), all its tokens
+  kGateUpStream = 2,    // moe_gate_up_stream: rows streamed by bulk copies through shared memory
+};
+
 // Compile-time shape of one kernel instance.
 struct GateUpPlan {
-  int npw;  // neurons per warp (gate + up rows: 2*npw rows in flight)
-  int cpl;  // MXFP8 blocks per lane per row per pass
+  int variant;  // GateUpVariant
+  int npw;      // neurons per warp (gate + up rows: 2*npw rows in flight)
+  int cpl;      // batched: MXFP8 blocks per lane per row per pass;
+                // rowshare: words (4 elements) dequantised per step, 1 or 2
+};
+enum DownVariant {
+  kDownBatched = 0,  // moe_down_3d_batched: one warp per (token, output-dim group)
+  kDownStream = 1,   // moe_down_stream: rows streamed by bulk copies, lane = token accumulator
 };
 struct DownPlan {
-  int rpw;  // output dims per warp
-  int qpl;  // virtual blocks (over all K routed rows) per lane per pass
+  int rpw;          // batched: output dims per warp
+  int qpl;          // batched: virtual blocks per lane per pass; stream: ring stages
+  int variant = 0;  // DownVariant
 };
 
-GateUpPlan plan_gate_up(int B, int H, int I, int K);
-DownPlan plan_down(int B, int H, int I, int K);
+GateUpPlan plan_gate_up(int B, int H, int I, int K, int E);
+DownPlan plan_down(int B, int H, int I, int K, int E);
+// The plans above, downgraded to a non-streamed kernel when the bulk copies'
+// 16-byte alignment does not hold for the given pointers.
+GateUpPlan plan_gate_up_for(const GateUpArgs& a);
+DownPlan plan_down_for(const DownArgs& a);
 
 cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_gate_up_rowshare(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                    bool pdl);
+cudaError_t launch_gate_up_stream(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                  bool pdl);
+bool gate_up_stream_supported(int B, int H, int I, int E, int K, int npw);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
+bool down_stream_supported(int B, int H, int I, int E, int K);
 
 }  // namespace wd

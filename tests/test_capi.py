@@ -126,3 +126,13 @@ def test_bench_kernels_reject_unaligned_buffers():
 
 def test_launch_count():
     assert wd.wd_moe_launches_per_call() == 2
+
+
+def test_plan_override_parser():
+    lib = wd.lib()
+    assert lib.wd_moe_set_plan(b"gu=rowshare:2:1,dn=4:1,rowshare_min_b=4") == OK
+    assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
+    assert lib.wd_moe_set_plan(b"nonsense") == INVALID
+    assert lib.wd_moe_set_plan(b"dn=2") == INVALID
+    assert lib.wd_moe_set_plan(None) == OK
+    assert lib.wd_moe_set_plan(b"") == OK

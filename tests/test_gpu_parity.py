@@ -217,3 +217,65 @@ def test_smaller_batch_reuses_a_larger_workspace(cuda_device):
         want = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, wl.I, wl.E)
         compare(from_dev_bf16(out), want, f"shared workspace B={B}")
     assert wd.wd_moe_read_error_flag(layer.workspace) == 0
+
+
+# every compiled kernel instance, selected through the plan override
+PLANS = [
+    "gu=batched:1:1,dn=1:1",
+    "gu=batched:1:2,dn=1:2",
+    "gu=batched:2:1,dn=2:1",
+    "gu=batched:2:1,dn=2:3",
+    "gu=rowshare:1:1,dn=4:1",
+    "gu=rowshare:1:2,dn=4:2",
+    "gu=rowshare:2:1,dn=2:2",
+    "gu=rowshare:2:2,dn=1:6",
+    "gu=batched:1:1,dn=1:4",
+    "gu=stream:2:2,dn=stream:8",
+    "gu=stream:1:2,dn=stream:3",
+    "gu=stream:3:3,dn=stream:2",
+]
+
+PLAN_SHAPES = [
+    (3, 288, 96, 5, 3, "uniform"),
+    (5, 1056, 160, 7, 2, "uniform"),
+    (2, 4096, 256, 4, 4, "uniform"),
+    (7, 2048, 2048, 6, 6, "uniform"),
+    (33, 512, 768, 16, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "fixed"),
+    (9, 512, 128, 8, 3, "uniform"),       # smallest shape both streamed kernels accept
+    (17, 1024, 832, 20, 5, "uniform"),    # I = 832: ragged lane slices in both
+]
+
+
+@pytest.fixture
+def plan_reset():
+    yield
+    wd.wd_moe_set_plan(None)
+
+
+@pytest.mark.parametrize("B,H,I,E,K,route", PLAN_SHAPES)
+def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
+    xs, ids, w, gu, gus, dn, dns = _random_case(300 + B + H + I + E, B, H, I, E, K, route=route)
+    want, want_h, _, _ = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, I, E, with_f64=True)
+    for plan in PLANS:
+        wd.wd_moe_set_plan(plan)
+        got, got_h, flag = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns)
+        compare(got_h.reshape(-1, I), want_h.reshape(-1, I), f"{plan} h")
+        compare(got, want, f"{plan} out")
+        assert flag == 0, plan
+
+
+@pytest.mark.parametrize("plan", ["gu=rowshare:2:2,rowshare_min_b=1,dn=2:3",
+                                  "gu=stream:2:3,dn=stream:8"])
+def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
+    wd.wd_moe_set_plan(plan)
+    xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
+    ids = ids.copy()
+    ids[0, 1], ids[4, 0], ids[8, 2] = -1, 8, 99
+    want, want_h, _, bad = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, 128, 8, with_f64=True)
+    got, got_h, flag = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns)
+    assert bad == 3 and flag == 1
+    assert not got_h[0, 1].any() and not got_h[4, 0].any() and not got_h[8, 2].any()
+    compare(got_h.reshape(-1, 128), want_h.reshape(-1, 128), "rowshare bad ids h")
+    compare(got, want, "rowshare bad ids")
