@@ -21,7 +21,8 @@ namespace wd {
 //
 // wd_moe_set_plan (or the WD_PLAN environment variable, read at the first
 // call) overrides the choice for tuning sweeps and tests:
-//   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>",
+//   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
+//   "gu=mixed:<npw>:<stages>",
 //   "dn=<rpw>:<qpl>" | "dn=stream:<stages>",
 //   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
 namespace {
@@ -43,6 +44,10 @@ bool parse_plan(const char* spec, PlanOverride* out) {
       int a = 0, b = 0;
       if (sscanf(tok, "gu=batched:%d:%d", &a, &b) == 2) {
         p.gu_variant = kGateUpBatched;
+        p.gu_npw = a;
+        p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=mixed:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpMixed;
         p.gu_npw = a;
         p.gu_cpl = b;
       } else if (sscanf(tok, "gu=stream:%d:%d", &a, &b) == 2) {
@@ -87,6 +92,8 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
   const bool rowshare_ok = B * K <= kRowShareMaxSlots && E <= kRowShareMaxExperts;
   if (o.gu_variant == kGateUpStream && gate_up_stream_supported(B, H, I, E, K, o.gu_npw))
     return {kGateUpStream, o.gu_npw, o.gu_cpl};
+  if (o.gu_variant == kGateUpMixed && gate_up_mixed_supported(B, H, I, E, K, o.gu_npw))
+    return {kGateUpMixed, o.gu_npw, o.gu_cpl};
   if (o.gu_variant == kGateUpRowShare && rowshare_ok) return {kGateUpRowShare, o.gu_npw, o.gu_cpl};
   if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
   // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack: one
@@ -111,7 +118,8 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
   GateUpPlan p = plan_gate_up(a.B, a.H, a.I, a.K, a.E);
-  if (p.variant == kGateUpStream && !(aligned16(a.gate_up) && aligned16(a.gate_up_scale)))
+  if ((p.variant == kGateUpStream || p.variant == kGateUpMixed) &&
+      !(aligned16(a.gate_up) && aligned16(a.gate_up_scale)))
     p = {kGateUpBatched, 2, 1};
   return p;
 }

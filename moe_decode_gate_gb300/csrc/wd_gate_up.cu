@@ -131,6 +131,7 @@ cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_
                            bool pdl) {
   if (p.variant == kGateUpRowShare) return launch_gate_up_rowshare(a, p, stream, pdl);
   if (p.variant == kGateUpStream) return launch_gate_up_stream(a, p, stream, pdl);
+  if (p.variant == kGateUpMixed) return launch_gate_up_mixed(a, p, stream, pdl);
 #define WD_GU_CASE(NPW, CPL) \
   if (p.npw == NPW && p.cpl == CPL) return launch_gate_up_t<NPW, CPL>(a, stream, pdl);
   WD_GU_CASE(1, 1)

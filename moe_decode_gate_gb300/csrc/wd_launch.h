@@ -37,6 +37,7 @@ enum GateUpVariant {
   kGateUpBatched = 0,   // moe_gate_up_3d_batched: one warp per (token, slot, neuron group)
   kGateUpRowShare = 1,  // moe_gate_up_rowshare: one warp per (expert, neuron group), all its tokens
   kGateUpStream = 2,    // moe_gate_up_stream: rows streamed by bulk copies through shared memory
+  kGateUpMixed = 3,     // moe_gate_up_mixed: streamed rows, FP16 x FP16 -> FP32 products
 };
 
 // Compile-time shape of one kernel instance.
@@ -69,6 +70,9 @@ cudaError_t launch_gate_up_rowshare(const GateUpArgs& a, const GateUpPlan& p, cu
 cudaError_t launch_gate_up_stream(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                   bool pdl);
 bool gate_up_stream_supported(int B, int H, int I, int E, int K, int npw);
+cudaError_t launch_gate_up_mixed(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                 bool pdl);
+bool gate_up_mixed_supported(int B, int H, int I, int E, int K, int npw);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_stream_supported(int B, int H, int I, int E, int K);

@@ -89,6 +89,11 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   return p;
 }
 
+// Barrier among `count` threads (a multiple of 32) of the CTA, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ uint2 lds_u32x2(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));

@@ -233,6 +233,9 @@ PLANS = [
     "gu=stream:2:2,dn=stream:8",
     "gu=stream:1:2,dn=stream:3",
     "gu=stream:3:3,dn=stream:2",
+    "gu=mixed:1:2,dn=4:1",
+    "gu=mixed:3:2,dn=2:3",
+    "gu=mixed:2:2,dn=2:2",
 ]
 
 PLAN_SHAPES = [
@@ -279,3 +282,22 @@ def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     assert not got_h[0, 1].any() and not got_h[4, 0].any() and not got_h[8, 2].any()
     compare(got_h.reshape(-1, 128), want_h.reshape(-1, 128), "rowshare bad ids h")
     compare(got, want, "rowshare bad ids")
+
+
+@pytest.mark.parametrize("plan", ["gu=mixed:1:2", "gu=mixed:3:2", "gu=mixed:2:2"])
+def test_fp16_product_path_keeps_tokens_fp16_cannot_hold_exact(cuda_device, plan_reset, plan):
+    """The mixed-precision gate/up kernel multiplies in FP16 only for tokens
+    whose BF16 activations are all exactly representable in FP16; the others
+    must take the FP32 path.  Tokens here: ordinary; one tiny (1e-30) element;
+    one element above the FP16 range; all zeros; an element at 2^-17 (still
+    exact); an element at 2^-18 (not exact)."""
+    wd.wd_moe_set_plan(plan)
+    xs, ids, w, gu, gus, dn, dns = _random_case(21, 6, 1024, 256, 8, 3)
+    xf = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).float()
+    xf[1, 17] = 1e-30
+    xf[2, 900] = 7.0e4
+    xf[3, :] = 0.0
+    xf[4, 5] = 2.0 ** -17
+    xf[5, 1000] = 2.0 ** -18
+    xs = xf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"{plan} fp16 boundary tokens")
