@@ -22,15 +22,15 @@ namespace wd {
 // wd_moe_set_plan (or the WD_PLAN environment variable, read at the first
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
-//   "gu=mixed:<npw>:<stages>",
-//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>",
+//   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<sbw>",
+//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>",
 //   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
 namespace {
 
 struct PlanOverride {
   int gu_variant = -1, gu_npw = 0, gu_cpl = 0;
   int dn_variant = -1, dn_rpw = 0, dn_qpl = 0;
-  int rowshare_min_b = 16;
+  int rowshare_min_b = 16;  // shared-row kernel where the persistent one does not apply
 };
 
 bool parse_plan(const char* spec, PlanOverride* out) {
@@ -54,6 +54,10 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpStream;
         p.gu_npw = a;
         p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=persist:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpPersist;
+        p.gu_npw = a;
+        p.gu_cpl = b;
       } else if (sscanf(tok, "gu=rowshare:%d:%d", &a, &b) == 2) {
         p.gu_variant = kGateUpRowShare;
         p.gu_npw = a;
@@ -61,6 +65,10 @@ bool parse_plan(const char* spec, PlanOverride* out) {
       } else if (sscanf(tok, "dn=stream:%d", &a) == 1) {
         p.dn_variant = kDownStream;
         p.dn_qpl = a;
+      } else if (sscanf(tok, "dn=persist:%d:%d", &a, &b) == 2) {
+        p.dn_variant = kDownPersist;
+        p.dn_rpw = a;
+        p.dn_qpl = b;
       } else if (sscanf(tok, "dn=%d:%d", &a, &b) == 2) {
         p.dn_variant = kDownBatched;
         p.dn_rpw = a;
@@ -95,11 +103,16 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
   if (o.gu_variant == kGateUpMixed && gate_up_mixed_supported(B, H, I, E, K, o.gu_npw))
     return {kGateUpMixed, o.gu_npw, o.gu_cpl};
   if (o.gu_variant == kGateUpRowShare && rowshare_ok) return {kGateUpRowShare, o.gu_npw, o.gu_cpl};
+  if (o.gu_variant == kGateUpPersist && gate_up_persist_supported(B, H, I, E, K))
+    return {kGateUpPersist, o.gu_npw, o.gu_cpl};
   if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
-  // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack: one
-  // warp per (token, slot, neuron pair) while tokens rarely share experts; one
-  // dequantised row per expert for all its tokens once they do
+  // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack
+  // (H=2048, I=768, E=128, K=8): one warp per (token, slot, neuron group) while
+  // tokens rarely share experts (2*B*K < E); one wave of persistent CTAs, each
+  // expert row dequantised once for all its tokens, once they do.
+  if (2 * B * K >= E && gate_up_persist_supported(B, H, I, E, K)) return {kGateUpPersist, 2, 2};
   if (rowshare_ok && B >= o.rowshare_min_b) return {kGateUpRowShare, 2, 2};
+  if (B == 1) return {kGateUpBatched, 1, 1};
   return {kGateUpBatched, 2, 1};  // two passes of 1 KiB per row at H=2048, 4 rows in flight
 }
 
@@ -108,9 +121,13 @@ DownPlan plan_down(int B, int H, int I, int K, int E) {
   if (o.dn_variant == kDownStream && down_stream_supported(B, H, I, E, K))
     return DownPlan{0, o.dn_qpl, kDownStream};
   if (o.dn_variant == kDownBatched) return DownPlan{o.dn_rpw, o.dn_qpl, kDownBatched};
-  if (B >= 8) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
+  if (o.dn_variant == kDownPersist) return DownPlan{o.dn_rpw, o.dn_qpl, kDownPersist};
+  if (B >= 4) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
   const int nq = K * (I / 32);
   const int per_lane = (nq + 31) / 32;
+  if (B == 1)  // one output dim per warp, all of its K rows in flight at once
+    return DownPlan{1, per_lane >= 6 ? 6 : (per_lane >= 4 ? 4 : (per_lane >= 2 ? 2 : 1)),
+                    kDownBatched};
   return DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
 }
 

@@ -25,31 +25,39 @@ struct U32x8 {
   uint32_t v[8];
 };
 
+// The load helpers below are plain (non-volatile) asm with no memory clobber,
+// so the compiler may schedule them freely: hoist them above arithmetic, batch
+// them and overlap their latencies.  Weights and scales are read-only for the
+// whole launch, so that is always safe.  Activations may be written by the
+// kernel before this one on the stream: their addresses must carry the token
+// returned by grid_dependency_wait() (a zero that the compiler cannot see
+// through), which keeps every such load after the wait.
+
 // 32 bytes of a weight row: read-only for the kernel's lifetime, no L1 allocation.
 __device__ __forceinline__ U32x8 ld_weights_32B(const void* p) {
   U32x8 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]),
                  "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
                : "l"(p));
   return r;
 }
 
-// 32 bytes of an activation vector (written by an earlier kernel): coherent load.
+// 32 bytes of an activation vector (written by an earlier kernel): coherent
+// load; `p` must depend on grid_dependency_wait()'s token.
 __device__ __forceinline__ U32x8 ld_act_32B(const void* p) {
   U32x8 r;
-  asm volatile("ld.global.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]),
-                 "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
-               : "l"(p)
-               : "memory");
+  asm("ld.global.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]), "=r"(r.v[5]),
+        "=r"(r.v[6]), "=r"(r.v[7])
+      : "l"(p));
   return r;
 }
 
 // One scale byte, read-only, no L1 allocation.
 __device__ __forceinline__ uint32_t ld_scale(const uint8_t* p) {
   uint16_t r;
-  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
   return r;
 }
 
@@ -109,8 +117,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Programmatic dependent launch controls (no-ops when launched without it).
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+// The wait returns a token equal to 0; adding it to an activation address
+// makes that load data-dependent on the wait.
+__device__ __forceinline__ uint32_t grid_dependency_wait() {
+  uint32_t token;
+  asm volatile("griddepcontrol.wait;\n\tmov.u32 %0, 0;" : "=r"(token) : : "memory");
+  return token;
 }
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256, 2) moe_gate_up_3d_batched(
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I,
     int E, int K) {
   // x and topk_ids may come from the kernel before this one on the stream.
-  grid_dependency_wait();
+  const uint32_t wait_token = grid_dependency_wait();
   grid_launch_dependents();
 
   const int lane = threadIdx.x & 31;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256, 2) moe_gate_up_3d_batched(
   const int nblk = H >> 5;  // MXFP8 blocks per row
   const size_t gate_row0 = (size_t)e * 2 * I + n0;
   const size_t up_row0 = gate_row0 + I;
-  const uint8_t* xrow = reinterpret_cast<const uint8_t*>(x + (size_t)b * H);
+  const uint8_t* xrow = reinterpret_cast<const uint8_t*>(x + (size_t)b * H) + wait_token;
 
   float accg[NPW], accu[NPW];
 #pragma unroll
@@ -132,6 +132,7 @@ cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_
   if (p.variant == kGateUpRowShare) return launch_gate_up_rowshare(a, p, stream, pdl);
   if (p.variant == kGateUpStream) return launch_gate_up_stream(a, p, stream, pdl);
   if (p.variant == kGateUpMixed) return launch_gate_up_mixed(a, p, stream, pdl);
+  if (p.variant == kGateUpPersist) return launch_gate_up_persist(a, p, stream, pdl);
 #define WD_GU_CASE(NPW, CPL) \
   if (p.npw == NPW && p.cpl == CPL) return launch_gate_up_t<NPW, CPL>(a, stream, pdl);
   WD_GU_CASE(1, 1)

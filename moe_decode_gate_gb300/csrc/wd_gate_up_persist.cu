@@ -1,0 +1,328 @@
+// wd_gate_up_persist.cu - moe_gate_up_persist: the gate/up kernel as one wave
+// of persistent CTAs over shared expert rows.
+//
+// Computes what moe_gate_up_3d_batched computes (Cursor, "用 warp decode 实现
+// 更好的 MoE 模型推理", section 两个 kernel 如何工作, gate/up paragraph): for
+// every (token, routed slot) and intermediate neuron n, the dot products of
+// gate row n and up row I+n of the routed expert with x, then one BF16 value
+// bf16(SiLU(g) * u).  Each output is still produced by exactly one warp, with
+// no padding, no activation scatter and no combine pass.  What is organised
+// differently, for batches in which tokens share experts:
+//
+//   - a warp owns NPW=2 neurons of one routed expert (4 rows) and produces them
+//     for every token routed to that expert, so each weight row is read from
+//     HBM and dequantised once per call;
+//   - the grid is one wave of CTAs.  Each CTA builds the routing tables once
+//     (routed experts ascending, their (token, slot) lists), then walks a
+//     contiguous range of (expert, 16-neuron block) items.  Ranges are cut so
+//     that every CTA gets the same estimated cost (items of an expert with T
+//     tokens cost T + kItemBase units), so experts with many tokens do not
+//     leave a tail;
+//   - when a CTA moves to a new expert it stages that expert's tokens' x rows
+//     in shared memory once, converted to FP32, in a layout whose 16-byte
+//     chunks are XOR-swizzled by block so that the lanes of a warp (one MXFP8
+//     block each) read them without bank conflicts.  The dot products then
+//     read activations from shared memory with no conversion;
+//   - the E8M0 block scale multiplies each 32-element partial sum rather than
+//     every element (exact for a power of two barring FP32 over/underflow);
+//   - the 4*TC partial sums of a chunk of TC tokens are reduced across the
+//     warp by a transpose-reduction (each shuffle step halves the number of
+//     values per lane), after which lane pairs hold gate and up of one output.
+#include "wd_device.cuh"
+#include "wd_launch.h"
+#include "wd_pipeline.cuh"
+#include "wd_routing.cuh"
+
+namespace wd {
+
+namespace {
+
+constexpr int kPWarps = 8;
+constexpr int kPThreads = 32 * kPWarps;
+constexpr int kPNpw = 2;                       // neurons per warp
+constexpr int kPNeurons = kPWarps * kPNpw;     // neurons per item
+constexpr int kItemBase = 3;                   // item cost = T + kItemBase
+constexpr int kXMaxTokens = 8;                 // x rows staged at once (upper bound)
+constexpr int kXBudget = 96 * 1024;            // shared-memory bytes for staged x
+
+__host__ __device__ inline int persist_x_tokens(int H) {
+  const int t = kXBudget / (H * 4);
+  return t < 1 ? 1 : (t > kXMaxTokens ? kXMaxTokens : t);
+}
+
+// Staged x starts on a 128-byte boundary after the routing tables (its
+// 16-byte vector accesses need at least 16-byte alignment).
+constexpr int kXOffset = (routing_table_bytes() + 127) / 128 * 128;
+static_assert(kXOffset % 16 == 0 && kXOffset >= routing_table_bytes(), "staged x alignment");
+
+__host__ __device__ inline int persist_smem_bytes(int H) {
+  return kXOffset + persist_x_tokens(H) * H * 4;
+}
+
+// Shared-memory byte offset of 16-byte chunk c (elements 4c..4c+3) of MXFP8
+// block `blk` of staged token t.
+__device__ __forceinline__ uint32_t xs_chunk(uint32_t xs, int t, int H, int blk, int c) {
+  return xs + (uint32_t)(t * H + blk * 32) * 4u + (uint32_t)((c ^ (blk & 7)) << 4);
+}
+
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// Sum over the warp of V = 4*TCP values per lane (TCP a power of two), by
+// transpose-reduction: lane l ends with the sum of value index l >> (5 - log2 V).
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V]) {
+  constexpr int L = V == 4 ? 2 : (V == 8 ? 3 : 4);
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < L; ++k) {
+    const int off = 16 >> k;
+    const int n = V >> k;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (int off = 16 >> L; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  return s;
+}
+
+// One chunk of TC (<= 4) tokens for this warp's 2 neurons: dots of the 4 rows
+// (gate n0, gate n0+1, up n0, up n0+1) with the staged x of tokens t0..t0+TC-1,
+// reduction, SiLU(g)*u, one BF16 store per output.
+template <int TC>
+__device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_up,
+                                              const uint8_t* __restrict__ gate_up_scale,
+                                              __nv_bfloat16* __restrict__ h, uint32_t xs,
+                                              const int* __restrict__ slots, int t0,
+                                              size_t gate_row0, int n0, int H, int I) {
+  constexpr int TCP = TC == 3 ? 4 : TC;
+  const int lane = threadIdx.x & 31;
+  const int nblk = H >> 5;
+  // rows r = 0..3: gate n0, gate n0+1, up n0, up n0+1
+  const uint8_t* wbase = gate_up + gate_row0 * H;
+  const uint8_t* sbase = gate_up_scale + gate_row0 * nblk;
+  const size_t wup = (size_t)I * H;
+  const int sup = I * nblk;
+  float acc[TCP][4];
+#pragma unroll
+  for (int t = 0; t < TCP; ++t)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[t][r] = 0.0f;
+
+  for (int blk = lane; blk < nblk; blk += 32) {
+    U32x8 wv[4];
+    float sc[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      wv[r] = ld_weights_32B(wbase + (r >> 1) * wup + (r & 1) * H + blk * 32);
+      sc[r] = e8m0_to_f32(ld_scale(sbase + (r >> 1) * sup + (r & 1) * nblk + blk));
+    }
+    float2 p[TC][4];
+#pragma unroll
+    for (int t = 0; t < TC; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) p[t][r] = make_float2(0.f, 0.f);
+    const uint32_t xb = xs + (uint32_t)(t0 * H + blk * 32) * 4u;
+    const int sw = blk & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float2 wf[4][2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) e4m3x4_to_f32(wv[r].v[c], wf[r][0], wf[r][1]);
+      const uint32_t xc = xb + (uint32_t)((c ^ sw) << 4);
+#pragma unroll
+      for (int t = 0; t < TC; ++t) {
+        const float4 xv = lds_f32x4(xc + (uint32_t)(t * H * 4));
+        const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          p[t][r] = __ffma2_rn(wf[r][0], x01, p[t][r]);
+          p[t][r] = __ffma2_rn(wf[r][1], x23, p[t][r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TC; ++t)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[t][r] = fmaf(p[t][r].x + p[t][r].y, sc[r], acc[t][r]);
+  }
+
+  // value index t*4 + r; after the reduction lane l holds index l >> (5 - L)
+  constexpr int V = 4 * TCP;
+  constexpr int L = V == 4 ? 2 : (V == 8 ? 3 : 4);
+  float v[V];
+#pragma unroll
+  for (int t = 0; t < TCP; ++t)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[t * 4 + r] = acc[t][r];
+  const float s = transpose_reduce<V>(v);
+  const float up = __shfl_xor_sync(0xFFFFFFFFu, s, 2 << (5 - L));  // index bit 1: gate/up
+  const int idx = lane >> (5 - L);
+  const int t = idx >> 2, r = idx & 3;
+  if ((lane & ((1 << (5 - L)) - 1)) == 0 && (r & 2) == 0 && t < TC)
+    h[(size_t)slots[t] * I + n0 + (r & 1)] = __float2bfloat16_rn(silu(s) * up);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPThreads, 2) moe_gate_up_persist(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_ids,
+    const uint8_t* __restrict__ gate_up, const uint8_t* __restrict__ gate_up_scale,
+    __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I,
+    int E, int K) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const RoutingTables rt = routing_tables_at(smem);
+  const uint32_t xs = smem_u32(smem + kXOffset);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int BK = B * K;
+  const int xtok = persist_x_tokens(H);
+
+  // x and topk_ids may come from the kernel before this one on the stream.
+  const uint32_t wait_token = grid_dependency_wait();
+  grid_launch_dependents();
+  build_routing_tables(rt, topk_ids, BK, E, 4, kPThreads);
+
+  // out-of-range ids: CTA 0 zeroes their h rows and raises the flag
+  if (rt.scalar[2] && blockIdx.x == 0) {
+    for (int s = 0; s < BK; ++s) {
+      const int e = rt.ids[s];
+      if (e < 0 || e >= E)
+        for (int n = tid; n < I; n += kPThreads) h[(size_t)s * I + n] = __float2bfloat16_rn(0.0f);
+    }
+    if (tid == 0 && error_flag) atomicOr(error_flag, 1u);
+  }
+
+  // cost prefix over routed experts: item of expert u costs T_u + kItemBase,
+  // and expert u has nb items.  `coff` ([S + 1], unused here) holds the prefix.
+  const int U = rt.scalar[0];
+  const int nb = (I + kPNeurons - 1) / kPNeurons;
+  int* pc = rt.coff;  // [U + 1]
+  if (warp == 0) {
+    const int lane = tid & 31;
+    int base = 0;
+    for (int u0 = 0; u0 < U; u0 += 32) {
+      const int u = u0 + lane;
+      const int c = u < U ? nb * (rt.off[u + 1] - rt.off[u] + kItemBase) : 0;
+      int excl, total;
+      warp_exclusive_scan(c, excl, total);
+      if (u < U) pc[u] = base + excl;
+      base += total;
+    }
+    if (lane == 0) pc[U] = base;
+  }
+  __syncthreads();
+  const long long total = pc[U];
+  const int lo = (int)(total * blockIdx.x / gridDim.x);
+  const int hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  if (lo >= hi) return;
+
+  // first expert whose cost range reaches lo
+  int u = 0;
+  {
+    int a = 0, b = U - 1;
+    while (a < b) {  // largest u with pc[u] <= lo
+      const int m = (a + b + 1) >> 1;
+      if (pc[m] <= lo) a = m; else b = m - 1;
+    }
+    u = a;
+  }
+  const uint8_t* xg = reinterpret_cast<const uint8_t*>(x) + wait_token;
+  for (; u < U && pc[u] < hi; ++u) {
+    const int T = rt.off[u + 1] - rt.off[u];
+    const int cu = T + kItemBase;
+    // items g of expert u whose cost start pc[u] + g*cu lies in [lo, hi)
+    const int g0 = pc[u] >= lo ? 0 : (lo - pc[u] + cu - 1) / cu;
+    const int g1 = min(nb, (hi - pc[u] + cu - 1) / cu);
+    if (g0 >= g1) continue;
+    const int* slots = rt.slots + rt.off[u];
+    const size_t expert_row0 = (size_t)rt.expert[u] * 2 * I;
+    for (int q0 = 0; q0 < T; q0 += xtok) {
+      const int nq = min(xtok, T - q0);
+      // stage x of tokens q0..q0+nq-1 as FP32, swizzled (all warps)
+      __syncthreads();  // the previous group's x is no longer read
+      const int units = nq * (H >> 2);  // 16-byte FP32 chunks
+      for (int i = tid; i < units; i += kPThreads) {
+        const int t = i / (H >> 2);
+        const int k = i - t * (H >> 2);  // chunk index within the row: block k>>3, chunk k&7
+        const int b = slots[q0 + t] / K;
+        const uint2 raw = *reinterpret_cast<const uint2*>(xg + ((size_t)b * H + (size_t)k * 4) * 2);
+        const float2 lo2 = bf16x2_to_f32(raw.x), hi2 = bf16x2_to_f32(raw.y);
+        const uint32_t a = xs_chunk(xs, t, H, k >> 3, k & 7);
+        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(lo2.x), "f"(lo2.y),
+                     "f"(hi2.x), "f"(hi2.y)
+                     : "memory");
+      }
+      __syncthreads();
+      for (int g = g0; g < g1; ++g) {
+        const int n0 = (g * kPWarps + warp) * kPNpw;
+        if (n0 >= I) continue;  // partial last block (I % 16 != 0)
+        const size_t gate_row0 = expert_row0 + n0;
+        for (int c0 = 0; c0 < nq; c0 += 4) {
+          const int tc = min(4, nq - c0);
+          const int* sl = slots + q0 + c0;
+          if (tc == 4)
+            persist_chunk<4>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+          else if (tc == 3)
+            persist_chunk<3>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+          else if (tc == 2)
+            persist_chunk<2>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+          else
+            persist_chunk<1>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+        }
+      }
+    }
+  }
+}
+
+bool gate_up_persist_supported(int B, int H, int I, int E, int K) {
+  return B * K <= kStreamMaxSlots && E <= 4096 && H % 32 == 0 && I % 2 == 0 &&
+         persist_smem_bytes(H) <= 113 * 1024;
+}
+
+cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                   bool pdl) {
+  (void)p;
+  if (!gate_up_persist_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+  const int smem = persist_smem_bytes(a.H);
+  static int configured = 0;
+  if (configured < smem) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        moe_gate_up_persist, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_gate_up_persist, kPThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(per_sm * sms));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_gate_up_persist, reinterpret_cast<const __nv_bfloat16*>(a.x),
+                            a.topk_ids, a.gate_up, a.gate_up_scale,
+                            reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag, a.B, a.H, a.I,
+                            a.E, a.K);
+}
+
+}  // namespace wd

@@ -22,18 +22,16 @@
 
 namespace wd {
 
+// Activation loads; `p` carries grid_dependency_wait()'s token (see wd_device.cuh).
 __device__ __forceinline__ uint4 ld_act_16B(const void* p) {
   uint4 r;
-  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p)
-               : "memory");
+  asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
 
 __device__ __forceinline__ uint2 ld_act_8B(const void* p) {
   uint2 r;
-  asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");
+  asm("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
   return r;
 }
 
@@ -133,7 +131,7 @@ __global__ void __launch_bounds__(256, 2) moe_gate_up_rowshare(
   __shared__ int s_count, s_expert, s_bad;
 
   // x and topk_ids may come from the kernel before this one on the stream.
-  grid_dependency_wait();
+  const uint32_t wait_token = grid_dependency_wait();
   grid_launch_dependents();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -204,7 +202,7 @@ __global__ void __launch_bounds__(256, 2) moe_gate_up_rowshare(
   if (n0 >= I) return;
 
   const size_t gate_row0 = (size_t)e * 2 * I + n0;
-  const uint8_t* xb = reinterpret_cast<const uint8_t*>(x);
+  const uint8_t* xb = reinterpret_cast<const uint8_t*>(x) + wait_token;
   for (int c0 = 0; c0 < T; c0 += 4) {
     const int tc = min(4, T - c0);
     if (tc == 4)

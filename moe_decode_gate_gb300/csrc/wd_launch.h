@@ -38,6 +38,7 @@ enum GateUpVariant {
   kGateUpRowShare = 1,  // moe_gate_up_rowshare: one warp per (expert, neuron group), all its tokens
   kGateUpStream = 2,    // moe_gate_up_stream: rows streamed by bulk copies through shared memory
   kGateUpMixed = 3,     // moe_gate_up_mixed: streamed rows, FP16 x FP16 -> FP32 products
+  kGateUpPersist = 4,   // moe_gate_up_persist: one wave of CTAs over shared expert rows, x staged
 };
 
 // Compile-time shape of one kernel instance.
@@ -45,15 +46,16 @@ struct GateUpPlan {
   int variant;  // GateUpVariant
   int npw;      // neurons per warp (gate + up rows: 2*npw rows in flight)
   int cpl;      // batched: MXFP8 blocks per lane per row per pass;
-                // rowshare: words (4 elements) dequantised per step, 1 or 2
+                // rowshare, persist: words (4 elements) dequantised per step, 1 or 2
 };
 enum DownVariant {
   kDownBatched = 0,  // moe_down_3d_batched: one warp per (token, output-dim group)
   kDownStream = 1,   // moe_down_stream: rows streamed by bulk copies, lane = token accumulator
+  kDownPersist = 2,  // moe_down_3d_batched_persist: batched items walked by one wave of CTAs
 };
 struct DownPlan {
-  int rpw;          // batched: output dims per warp
-  int qpl;          // batched: virtual blocks per lane per pass; stream: ring stages
+  int rpw;          // batched, persist: output dims per warp
+  int qpl;          // batched, persist: virtual blocks per lane per pass; stream: ring stages
   int variant = 0;  // DownVariant
 };
 
@@ -73,6 +75,9 @@ bool gate_up_stream_supported(int B, int H, int I, int E, int K, int npw);
 cudaError_t launch_gate_up_mixed(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                  bool pdl);
 bool gate_up_mixed_supported(int B, int H, int I, int E, int K, int npw);
+cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                   bool pdl);
+bool gate_up_persist_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_stream_supported(int B, int H, int I, int E, int K);

@@ -89,6 +89,18 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   return p;
 }
 
+// Ask L2 to fetch the whole 16-byte chunks of [p, p + bytes) from HBM (no
+// registers, no shared memory, nothing to wait for).  The partial chunks at
+// either end are left out, so nothing outside the range is touched.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t lo = (a + 15u) & ~static_cast<uintptr_t>(15u);
+  const uintptr_t hi = (a + bytes) & ~static_cast<uintptr_t>(15u);
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo))
+                 : "memory");
+}
+
 // Barrier among `count` threads (a multiple of 32) of the CTA, id 1..15.
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -28,9 +28,8 @@ struct RoutingTables {
   int* scalar;     // [0] routed experts U, [1] chunks, [2] 1 if an id was out of range
 };
 
-__host__ __device__ inline int routing_table_bytes() {
-  const int S = kStreamMaxSlots;
-  return 4 * (128 + 128 + S + S + (S + 1) + (S + 1) + S + S + S + 8);
+__host__ __device__ constexpr int routing_table_bytes() {
+  return 4 * (128 + 128 + kStreamMaxSlots * 7 + 2 + 8);
 }
 
 __device__ __forceinline__ RoutingTables routing_tables_at(void* base) {

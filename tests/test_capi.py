@@ -132,6 +132,7 @@ def test_plan_override_parser():
     lib = wd.lib()
     assert lib.wd_moe_set_plan(b"gu=rowshare:2:1,dn=4:1,rowshare_min_b=4") == OK
     assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
+    assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=persist:4:1") == OK
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID
     assert lib.wd_moe_set_plan(None) == OK
