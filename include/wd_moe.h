@@ -138,14 +138,29 @@ WD_API int wd_moe_launches_per_call(void);
  * use).  `spec` is a comma-separated list of
  *   "gu=batched:<neurons per warp>:<blocks per lane per pass>"
  *   "gu=rowshare:<neurons per warp>:<words per step>"   (tokens share rows)
+ *   "gu=persist:<neurons per warp>:<1 + L2 prefetch distance>"
+ *   "gu=stream:<variant>:<stages>" | "gu=mixed:<variant>:<stages>"
  *   "dn=<output dims per warp>:<blocks per lane per pass>"
- *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel>"
+ *   "dn=persist:<output dims per warp>:<blocks per lane per pass>"
+ *   "dn=stream:<stages>" | "dn=shared:<output dims per CTA>"
+ *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel
+ *                    where the persistent one does not apply>"
  * NULL or "" restores the built-in plan.  Returns WD_ERR_INVALID_ARG for an
- * unparsable spec (the plan is then unchanged); an unsupported combination
- * makes later launches fail with WD_ERR_CUDA.  Process-wide; do not call while
- * another thread is inside a wd_moe_* call.  The WD_PLAN environment variable,
- * read at the first launch, sets the initial override. */
+ * unparsable spec (the plan is then unchanged); a variant that does not
+ * support the call's shape falls back to the built-in choice, and an
+ * unsupported parameter combination makes later launches fail with
+ * WD_ERR_CUDA.  Process-wide; do not call while another thread is inside a
+ * wd_moe_* call.  The WD_PLAN environment variable, read at the first launch,
+ * sets the initial override. */
 WD_API wd_status wd_moe_set_plan(const char* spec);
+
+/* Write the kernels wd_moe_decode would launch for this shape under the
+ * current plan (16-byte-aligned weight pointers assumed), as
+ * "gate_up=<kernel><params> down=<kernel><params>", NUL-terminated, into
+ * `buf` (`bytes` long; 128 bytes always suffice).  Host-only: launches
+ * nothing.  Returns WD_ERR_INVALID_ARG for a NULL or too small buffer and the
+ * status wd_moe_decode would return for invalid dimensions. */
+WD_API wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, size_t bytes);
 
 /* The same layer as wd_moe_decode, for callers that cannot allocate device
  * memory and so cannot provide a workspace: for example a plugin whose host

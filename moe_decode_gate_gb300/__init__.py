@@ -3,8 +3,11 @@
 Two hand-written sm_103a CUDA kernels behind a C-ABI (include/wd_moe.h):
 ``moe_gate_up_3d_batched`` (one warp per token x routed expert x neuron group)
 and ``moe_down_3d_batched`` (one warp per token x output-dim group, all K
-experts folded into one FP32 register accumulator).  This package is the thin
-Python binding over that library; PyTorch only supplies device memory and
+experts folded into one FP32 register accumulator); for batches whose tokens
+share experts the gate/up stage runs ``moe_gate_up_persist``, which reads and
+dequantises each routed expert row once for all of its tokens
+(``wd_moe_describe_plan`` names the kernels a shape gets).  This package is the
+thin Python binding over that library; PyTorch only supplies device memory and
 streams.
 
     from moe_decode_gate_gb300 import wd_moe_decode, wd_moe_workspace_size
@@ -21,6 +24,7 @@ from ._native import (  # noqa: F401
     wd_bench_spec_gbs,
     wd_moe_decode,
     wd_moe_decode_no_alloc,
+    wd_moe_describe_plan,
     wd_moe_down,
     wd_moe_gate_up,
     wd_moe_launches_per_call,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "wd_moe_launches_per_call": (_I, []),
     "wd_moe_decode_no_alloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_moe_set_plan": (_I, [ctypes.c_char_p]),
+    "wd_moe_describe_plan": (_I, [ctypes.c_int] * 5 + [ctypes.c_char_p, ctypes.c_size_t]),
     "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
@@ -162,6 +163,14 @@ def wd_moe_launches_per_call() -> int:
 def wd_moe_set_plan(spec=None):
     """Override the launch plan (see include/wd_moe.h); None restores the default."""
     _check("wd_moe_set_plan", lib().wd_moe_set_plan(None if spec is None else spec.encode()))
+
+
+def wd_moe_describe_plan(B, H, I, E, K) -> str:
+    """The kernels wd_moe_decode would launch for this shape, e.g.
+    "gate_up=moe_gate_up_persist<2,1> down=moe_down_3d_batched<4,1>"."""
+    buf = ctypes.create_string_buffer(256)
+    _check("wd_moe_describe_plan", lib().wd_moe_describe_plan(B, H, I, E, K, buf, 256))
+    return buf.value.decode()
 
 
 def wd_moe_decode_no_alloc(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out,

@@ -23,7 +23,7 @@ namespace wd {
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
 //   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<sbw>",
-//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>",
+//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>",
 //   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
 namespace {
 
@@ -65,6 +65,9 @@ bool parse_plan(const char* spec, PlanOverride* out) {
       } else if (sscanf(tok, "dn=stream:%d", &a) == 1) {
         p.dn_variant = kDownStream;
         p.dn_qpl = a;
+      } else if (sscanf(tok, "dn=shared:%d", &a) == 1) {
+        p.dn_variant = kDownShared;
+        p.dn_rpw = a;
       } else if (sscanf(tok, "dn=persist:%d:%d", &a, &b) == 2) {
         p.dn_variant = kDownPersist;
         p.dn_rpw = a;
@@ -110,7 +113,7 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
   // (H=2048, I=768, E=128, K=8): one warp per (token, slot, neuron group) while
   // tokens rarely share experts (2*B*K < E); one wave of persistent CTAs, each
   // expert row dequantised once for all its tokens, once they do.
-  if (2 * B * K >= E && gate_up_persist_supported(B, H, I, E, K)) return {kGateUpPersist, 2, 2};
+  if (2 * B * K >= E && gate_up_persist_supported(B, H, I, E, K)) return {kGateUpPersist, 2, 1};
   if (rowshare_ok && B >= o.rowshare_min_b) return {kGateUpRowShare, 2, 2};
   if (B == 1) return {kGateUpBatched, 1, 1};
   return {kGateUpBatched, 2, 1};  // two passes of 1 KiB per row at H=2048, 4 rows in flight
@@ -122,6 +125,8 @@ DownPlan plan_down(int B, int H, int I, int K, int E) {
     return DownPlan{0, o.dn_qpl, kDownStream};
   if (o.dn_variant == kDownBatched) return DownPlan{o.dn_rpw, o.dn_qpl, kDownBatched};
   if (o.dn_variant == kDownPersist) return DownPlan{o.dn_rpw, o.dn_qpl, kDownPersist};
+  if (o.dn_variant == kDownShared && down_shared_supported(B, H, I, E, K, o.dn_rpw))
+    return DownPlan{o.dn_rpw, 0, kDownShared};
   if (B >= 4) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
   const int nq = K * (I / 32);
   const int per_lane = (nq + 31) / 32;
@@ -278,6 +283,23 @@ wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_str
 }
 
 int wd_moe_launches_per_call(void) { return 2; }
+
+wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, size_t bytes) {
+  if (!buf || bytes < 128) return WD_ERR_INVALID_ARG;
+  const wd_status st = check_dims(B, H, I, E, K);
+  if (st != WD_OK) return st;
+  const wd::GateUpPlan g = wd::plan_gate_up(B, H, I, K, E);
+  const wd::DownPlan d = wd::plan_down(B, H, I, K, E);
+  static const char* const gu_names[] = {"moe_gate_up_3d_batched", "moe_gate_up_rowshare",
+                                         "moe_gate_up_stream", "moe_gate_up_mixed",
+                                         "moe_gate_up_persist"};
+  static const char* const dn_names[] = {"moe_down_3d_batched", "moe_down_stream",
+                                         "moe_down_3d_batched_persist", "moe_down_shared"};
+  const char* gn = (g.variant >= 0 && g.variant <= 4) ? gu_names[g.variant] : "?";
+  const char* dn = (d.variant >= 0 && d.variant <= 3) ? dn_names[d.variant] : "?";
+  snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d>", gn, g.npw, g.cpl, dn, d.rpw, d.qpl);
+  return WD_OK;
+}
 
 wd_status wd_moe_set_plan(const char* spec) {
   wd::PlanOverride p;

@@ -9,12 +9,12 @@
 // no padding, no activation scatter and no combine pass.  What is organised
 // differently, for batches in which tokens share experts:
 //
-//   - a warp owns NPW=2 neurons of one routed expert (4 rows) and produces them
+//   - a warp owns NPW (1 or 2) neurons of one routed expert and produces them
 //     for every token routed to that expert, so each weight row is read from
 //     HBM and dequantised once per call;
 //   - the grid is one wave of CTAs.  Each CTA builds the routing tables once
 //     (routed experts ascending, their (token, slot) lists), then walks a
-//     contiguous range of (expert, 16-neuron block) items.  Ranges are cut so
+//     contiguous range of (expert, 8*NPW-neuron block) items.  Ranges are cut so
 //     that every CTA gets the same estimated cost (items of an expert with T
 //     tokens cost T + kItemBase units), so experts with many tokens do not
 //     leave a tail;
@@ -39,8 +39,6 @@ namespace {
 
 constexpr int kPWarps = 8;
 constexpr int kPThreads = 32 * kPWarps;
-constexpr int kPNpw = 2;                       // neurons per warp
-constexpr int kPNeurons = kPWarps * kPNpw;     // neurons per item
 constexpr int kItemBase = 3;                   // item cost = T + kItemBase
 constexpr int kXMaxTokens = 8;                 // x rows staged at once (upper bound)
 constexpr int kXBudget = 96 * 1024;            // shared-memory bytes for staged x
@@ -73,11 +71,11 @@ __device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
   return v;
 }
 
-// Sum over the warp of V = 4*TCP values per lane (TCP a power of two), by
+// Sum over the warp of V values per lane (V a power of two, 2..16), by
 // transpose-reduction: lane l ends with the sum of value index l >> (5 - log2 V).
 template <int V>
 __device__ __forceinline__ float transpose_reduce(float (&v)[V]) {
-  constexpr int L = V == 4 ? 2 : (V == 8 ? 3 : 4);
+  constexpr int L = V == 2 ? 1 : (V == 4 ? 2 : (V == 8 ? 3 : 4));
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 0; k < L; ++k) {
@@ -97,56 +95,56 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V]) {
   return s;
 }
 
-// One chunk of TC (<= 4) tokens for this warp's 2 neurons: dots of the 4 rows
-// (gate n0, gate n0+1, up n0, up n0+1) with the staged x of tokens t0..t0+TC-1,
-// reduction, SiLU(g)*u, one BF16 store per output.
-template <int TC>
+// One chunk of TC (<= 4) tokens for this warp's NPW neurons: dots of its
+// 2*NPW rows (gate n0..n0+NPW-1, then up n0..n0+NPW-1) with the staged x of
+// tokens t0..t0+TC-1, reduction, SiLU(g)*u, one BF16 store per output.
+template <int NPW, int TC>
 __device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_up,
                                               const uint8_t* __restrict__ gate_up_scale,
                                               __nv_bfloat16* __restrict__ h, uint32_t xs,
                                               const int* __restrict__ slots, int t0,
                                               size_t gate_row0, int n0, int H, int I) {
+  constexpr int R = 2 * NPW;
   constexpr int TCP = TC == 3 ? 4 : TC;
   const int lane = threadIdx.x & 31;
   const int nblk = H >> 5;
-  // rows r = 0..3: gate n0, gate n0+1, up n0, up n0+1
   const uint8_t* wbase = gate_up + gate_row0 * H;
   const uint8_t* sbase = gate_up_scale + gate_row0 * nblk;
   const size_t wup = (size_t)I * H;
   const int sup = I * nblk;
-  float acc[TCP][4];
+  float acc[TCP][R];
 #pragma unroll
   for (int t = 0; t < TCP; ++t)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) acc[t][r] = 0.0f;
+    for (int r = 0; r < R; ++r) acc[t][r] = 0.0f;
 
   for (int blk = lane; blk < nblk; blk += 32) {
-    U32x8 wv[4];
-    float sc[4];
+    U32x8 wv[R];
+    float sc[R];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      wv[r] = ld_weights_32B(wbase + (r >> 1) * wup + (r & 1) * H + blk * 32);
-      sc[r] = e8m0_to_f32(ld_scale(sbase + (r >> 1) * sup + (r & 1) * nblk + blk));
+    for (int r = 0; r < R; ++r) {
+      wv[r] = ld_weights_32B(wbase + (r / NPW) * wup + (r % NPW) * H + blk * 32);
+      sc[r] = e8m0_to_f32(ld_scale(sbase + (r / NPW) * sup + (r % NPW) * nblk + blk));
     }
-    float2 p[TC][4];
+    float2 p[TC][R];
 #pragma unroll
     for (int t = 0; t < TC; ++t)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) p[t][r] = make_float2(0.f, 0.f);
+      for (int r = 0; r < R; ++r) p[t][r] = make_float2(0.f, 0.f);
     const uint32_t xb = xs + (uint32_t)(t0 * H + blk * 32) * 4u;
     const int sw = blk & 7;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      float2 wf[4][2];
+      float2 wf[R][2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) e4m3x4_to_f32(wv[r].v[c], wf[r][0], wf[r][1]);
+      for (int r = 0; r < R; ++r) e4m3x4_to_f32(wv[r].v[c], wf[r][0], wf[r][1]);
       const uint32_t xc = xb + (uint32_t)((c ^ sw) << 4);
 #pragma unroll
       for (int t = 0; t < TC; ++t) {
         const float4 xv = lds_f32x4(xc + (uint32_t)(t * H * 4));
         const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < R; ++r) {
           p[t][r] = __ffma2_rn(wf[r][0], x01, p[t][r]);
           p[t][r] = __ffma2_rn(wf[r][1], x23, p[t][r]);
         }
@@ -155,28 +153,32 @@ __device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_u
 #pragma unroll
     for (int t = 0; t < TC; ++t)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[t][r] = fmaf(p[t][r].x + p[t][r].y, sc[r], acc[t][r]);
+      for (int r = 0; r < R; ++r) acc[t][r] = fmaf(p[t][r].x + p[t][r].y, sc[r], acc[t][r]);
   }
 
-  // value index t*4 + r; after the reduction lane l holds index l >> (5 - L)
-  constexpr int V = 4 * TCP;
-  constexpr int L = V == 4 ? 2 : (V == 8 ? 3 : 4);
+  // value index t*R + r; after the reduction lane l holds index l >> (5 - L),
+  // and index bit log2(NPW) (gate/up) sits at lane bit 5 - L + log2(NPW)
+  constexpr int V = R * TCP;
+  constexpr int L = V == 2 ? 1 : (V == 4 ? 2 : (V == 8 ? 3 : 4));
   float v[V];
 #pragma unroll
   for (int t = 0; t < TCP; ++t)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) v[t * 4 + r] = acc[t][r];
+    for (int r = 0; r < R; ++r) v[t * R + r] = acc[t][r];
   const float s = transpose_reduce<V>(v);
-  const float up = __shfl_xor_sync(0xFFFFFFFFu, s, 2 << (5 - L));  // index bit 1: gate/up
+  const float up = __shfl_xor_sync(0xFFFFFFFFu, s, NPW << (5 - L));
   const int idx = lane >> (5 - L);
-  const int t = idx >> 2, r = idx & 3;
-  if ((lane & ((1 << (5 - L)) - 1)) == 0 && (r & 2) == 0 && t < TC)
-    h[(size_t)slots[t] * I + n0 + (r & 1)] = __float2bfloat16_rn(silu(s) * up);
+  const int t = idx / R, r = idx % R;
+  if ((lane & ((1 << (5 - L)) - 1)) == 0 && r < NPW && t < TC)
+    h[(size_t)slots[t] * I + n0 + r] = __float2bfloat16_rn(silu(s) * up);
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kPThreads, 2) moe_gate_up_persist(
+// PFD: items ahead whose rows lane 0 of each warp requests into L2
+// (cp.async.bulk.prefetch) before computing the current one; 0 = none.
+template <int NPW, int MINB, int PFD>
+__global__ void __launch_bounds__(kPThreads, MINB) moe_gate_up_persist(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const uint8_t* __restrict__ gate_up, const uint8_t* __restrict__ gate_up_scale,
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I,
@@ -184,9 +186,10 @@ __global__ void __launch_bounds__(kPThreads, 2) moe_gate_up_persist(
   extern __shared__ __align__(16) uint8_t smem[];
   const RoutingTables rt = routing_tables_at(smem);
   const uint32_t xs = smem_u32(smem + kXOffset);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BK = B * K;
   const int xtok = persist_x_tokens(H);
+  const int nblk = H >> 5;
 
   // x and topk_ids may come from the kernel before this one on the stream.
   const uint32_t wait_token = grid_dependency_wait();
@@ -206,10 +209,10 @@ __global__ void __launch_bounds__(kPThreads, 2) moe_gate_up_persist(
   // cost prefix over routed experts: item of expert u costs T_u + kItemBase,
   // and expert u has nb items.  `coff` ([S + 1], unused here) holds the prefix.
   const int U = rt.scalar[0];
-  const int nb = (I + kPNeurons - 1) / kPNeurons;
+  constexpr int kNeurons = kPWarps * NPW;  // neurons per item
+  const int nb = (I + kNeurons - 1) / kNeurons;
   int* pc = rt.coff;  // [U + 1]
   if (warp == 0) {
-    const int lane = tid & 31;
     int base = 0;
     for (int u0 = 0; u0 < U; u0 += 32) {
       const int u = u0 + lane;
@@ -264,21 +267,34 @@ __global__ void __launch_bounds__(kPThreads, 2) moe_gate_up_persist(
                      : "memory");
       }
       __syncthreads();
+      // this warp's rows (NPW gate, NPW up; each group contiguous) of item gp, into L2
+      auto prefetch_item = [&](int gp) {
+        const int np = (gp * kPWarps + warp) * NPW;
+        if (lane != 0 || gp >= g1 || np >= I) return;
+        const size_t r0 = expert_row0 + np;
+        prefetch_l2_bulk(gate_up + r0 * H, (uint32_t)(NPW * H));
+        prefetch_l2_bulk(gate_up + (r0 + I) * H, (uint32_t)(NPW * H));
+        prefetch_l2_bulk(gate_up_scale + r0 * nblk, (uint32_t)(NPW * nblk));
+        prefetch_l2_bulk(gate_up_scale + (r0 + I) * nblk, (uint32_t)(NPW * nblk));
+      };
+#pragma unroll
+      for (int k = 0; k < PFD; ++k) prefetch_item(g0 + k);
       for (int g = g0; g < g1; ++g) {
-        const int n0 = (g * kPWarps + warp) * kPNpw;
-        if (n0 >= I) continue;  // partial last block (I % 16 != 0)
+        if (PFD > 0) prefetch_item(g + PFD);
+        const int n0 = (g * kPWarps + warp) * NPW;
+        if (n0 >= I) continue;  // partial last block (I % (8*NPW) != 0)
         const size_t gate_row0 = expert_row0 + n0;
         for (int c0 = 0; c0 < nq; c0 += 4) {
           const int tc = min(4, nq - c0);
           const int* sl = slots + q0 + c0;
           if (tc == 4)
-            persist_chunk<4>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+            persist_chunk<NPW, 4>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
           else if (tc == 3)
-            persist_chunk<3>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+            persist_chunk<NPW, 3>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
           else if (tc == 2)
-            persist_chunk<2>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+            persist_chunk<NPW, 2>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
           else
-            persist_chunk<1>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
+            persist_chunk<NPW, 1>(gate_up, gate_up_scale, h, xs, sl, c0, gate_row0, n0, H, I);
         }
       }
     }
@@ -290,23 +306,21 @@ bool gate_up_persist_supported(int B, int H, int I, int E, int K) {
          persist_smem_bytes(H) <= 113 * 1024;
 }
 
-cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                                   bool pdl) {
-  (void)p;
-  if (!gate_up_persist_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+template <int NPW, int MINB, int PFD>
+static cudaError_t launch_persist_t(const GateUpArgs& a, cudaStream_t stream, bool pdl) {
   const int smem = persist_smem_bytes(a.H);
   static int configured = 0;
   if (configured < smem) {
     const cudaError_t e = cudaFuncSetAttribute(
-        moe_gate_up_persist, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        moe_gate_up_persist<NPW, MINB, PFD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_gate_up_persist, kPThreads, smem);
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, moe_gate_up_persist<NPW, MINB, PFD>, kPThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   cudaLaunchConfig_t cfg = {};
@@ -319,10 +333,21 @@ cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cud
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gate_up_persist, reinterpret_cast<const __nv_bfloat16*>(a.x),
-                            a.topk_ids, a.gate_up, a.gate_up_scale,
-                            reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag, a.B, a.H, a.I,
-                            a.E, a.K);
+  return cudaLaunchKernelEx(&cfg, moe_gate_up_persist<NPW, MINB, PFD>,
+                            reinterpret_cast<const __nv_bfloat16*>(a.x), a.topk_ids, a.gate_up,
+                            a.gate_up_scale, reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag,
+                            a.B, a.H, a.I, a.E, a.K);
+}
+
+// p.npw: neurons per warp (1: 3 CTAs per SM, 2: 2 CTAs per SM); p.cpl: L2
+// prefetch distance in items plus one (1: none, 2: one item ahead).
+cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                   bool pdl) {
+  if (!gate_up_persist_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+  if (p.npw == 1) return p.cpl == 2 ? launch_persist_t<1, 3, 1>(a, stream, pdl)
+                                    : launch_persist_t<1, 3, 0>(a, stream, pdl);
+  return p.cpl == 2 ? launch_persist_t<2, 2, 1>(a, stream, pdl)
+                    : launch_persist_t<2, 2, 0>(a, stream, pdl);
 }
 
 }  // namespace wd

@@ -52,6 +52,7 @@ enum DownVariant {
   kDownBatched = 0,  // moe_down_3d_batched: one warp per (token, output-dim group)
   kDownStream = 1,   // moe_down_stream: rows streamed by bulk copies, lane = token accumulator
   kDownPersist = 2,  // moe_down_3d_batched_persist: batched items walked by one wave of CTAs
+  kDownShared = 3,   // moe_down_shared: CTA per output-dim group, expert rows shared by tokens
 };
 struct DownPlan {
   int rpw;          // batched, persist: output dims per warp
@@ -81,5 +82,7 @@ bool gate_up_persist_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_stream_supported(int B, int H, int I, int E, int K);
+cudaError_t launch_down_shared(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
+bool down_shared_supported(int B, int H, int I, int E, int K, int rpw);
 
 }  // namespace wd

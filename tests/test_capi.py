@@ -128,11 +128,40 @@ def test_launch_count():
     assert wd.wd_moe_launches_per_call() == 2
 
 
+def test_built_in_plan_by_batch():
+    """The kernels the built-in plan picks on the Qwen-3-style shape (host only)."""
+    wd.wd_moe_set_plan(None)
+    q = dict(H=2048, I=768, E=128, K=8)
+    assert wd.wd_moe_describe_plan(1, **q) == \
+        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6>"
+    assert wd.wd_moe_describe_plan(2, **q) == \
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3>"
+    assert wd.wd_moe_describe_plan(4, **q) == \
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1>"
+    for B in (8, 16, 32):
+        assert wd.wd_moe_describe_plan(B, **q) == \
+            "gate_up=moe_gate_up_persist<2,1> down=moe_down_3d_batched<4,1>"
+    # B*K above the persistent kernel's routing tables: the shared-row kernel
+    assert wd.wd_moe_describe_plan(64, **q).startswith("gate_up=moe_gate_up_rowshare<2,2>")
+    wd.wd_moe_set_plan("gu=batched:1:2,dn=shared:4")
+    try:
+        assert wd.wd_moe_describe_plan(32, **q) == \
+            "gate_up=moe_gate_up_3d_batched<1,2> down=moe_down_shared<4,0>"
+    finally:
+        wd.wd_moe_set_plan(None)
+    lib = wd.lib()
+    buf = ctypes.create_string_buffer(64)
+    assert lib.wd_moe_describe_plan(32, 2048, 768, 128, 8, buf, 64) == INVALID
+    buf = ctypes.create_string_buffer(128)
+    assert lib.wd_moe_describe_plan(0, 2048, 768, 128, 8, buf, 128) == INVALID
+
+
 def test_plan_override_parser():
     lib = wd.lib()
     assert lib.wd_moe_set_plan(b"gu=rowshare:2:1,dn=4:1,rowshare_min_b=4") == OK
     assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
     assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=persist:4:1") == OK
+    assert lib.wd_moe_set_plan(b"gu=persist:1:1,dn=shared:2") == OK
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID
     assert lib.wd_moe_set_plan(None) == OK

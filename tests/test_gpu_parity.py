@@ -237,9 +237,12 @@ PLANS = [
     "gu=mixed:3:2,dn=2:3",
     "gu=mixed:2:2,dn=2:2",
     "gu=persist:2:2,dn=persist:4:1",
-    "gu=persist:2:2,dn=persist:2:1",
-    "gu=persist:2:2,dn=persist:2:3",
+    "gu=persist:2:1,dn=persist:2:1",
+    "gu=persist:1:1,dn=persist:2:3",
+    "gu=persist:1:2,dn=4:1",
     "gu=persist:2:2,dn=persist:1:6",
+    "gu=persist:2:2,dn=shared:4",
+    "gu=batched:2:1,dn=shared:2",
 ]
 
 PLAN_SHAPES = [
@@ -276,7 +279,8 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
 
 @pytest.mark.parametrize("plan", ["gu=rowshare:2:2,rowshare_min_b=1,dn=2:3",
                                   "gu=stream:2:3,dn=stream:8",
-                                  "gu=persist:2:2,dn=persist:4:1"])
+                                  "gu=persist:2:2,dn=persist:4:1",
+                                  "gu=persist:2:2,dn=shared:4"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
