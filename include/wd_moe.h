@@ -131,6 +131,10 @@ WD_API wd_status wd_moe_down(const void* h, const int32_t* topk_ids, const float
 WD_API wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes,
                                        wd_stream_t stream, int* flag);
 
+/* Name of the CUDA error (cudaGetErrorName) behind the calling thread's most
+ * recent WD_ERR_CUDA, or "none".  Static storage; never NULL. */
+WD_API const char* wd_last_error_string(void);
+
 /* Number of kernel launches wd_moe_decode issues per call (for accounting). */
 WD_API int wd_moe_launches_per_call(void);
 
@@ -139,6 +143,7 @@ WD_API int wd_moe_launches_per_call(void);
  *   "gu=batched:<neurons per warp>:<blocks per lane per pass>"
  *   "gu=rowshare:<neurons per warp>:<words per step>"   (tokens share rows)
  *   "gu=persist:<neurons per warp>:<1 + L2 prefetch distance>"
+ *   "gu=ring:<bulk-copy ring stages per warp>" | "gu=tma"
  *   "gu=stream:<variant>:<stages>" | "gu=mixed:<variant>:<stages>"
  *   "dn=<output dims per warp>:<blocks per lane per pass>"
  *   "dn=persist:<output dims per warp>:<blocks per lane per pass>"

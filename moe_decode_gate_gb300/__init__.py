@@ -25,6 +25,7 @@ from ._native import (  # noqa: F401
     wd_moe_decode,
     wd_moe_decode_no_alloc,
     wd_moe_describe_plan,
+    wd_last_error_string,
     wd_moe_down,
     wd_moe_gate_up,
     wd_moe_launches_per_call,

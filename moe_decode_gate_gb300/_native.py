@@ -34,6 +34,7 @@ SIGNATURES = {
     "wd_moe_launches_per_call": (_I, []),
     "wd_moe_decode_no_alloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_moe_set_plan": (_I, [ctypes.c_char_p]),
+    "wd_last_error_string": (ctypes.c_char_p, []),
     "wd_moe_describe_plan": (_I, [ctypes.c_int] * 5 + [ctypes.c_char_p, ctypes.c_size_t]),
     "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
@@ -44,9 +45,10 @@ SIGNATURES = {
 
 
 class WdError(RuntimeError):
-    def __init__(self, fn, status):
+    def __init__(self, fn, status, detail=None):
         self.status = status
-        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}")
+        extra = f" ({detail})" if detail else ""
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}{extra}")
 
 
 def library_path() -> str:
@@ -72,7 +74,10 @@ def lib() -> ctypes.CDLL:
 
 def _check(fn, status):
     if status != WD_OK:
-        raise WdError(fn, status)
+        detail = None
+        if STATUS_NAMES.get(status) == "WD_ERR_CUDA":
+            detail = lib().wd_last_error_string().decode()
+        raise WdError(fn, status, detail)
 
 
 def _stream(stream):
@@ -163,6 +168,11 @@ def wd_moe_launches_per_call() -> int:
 def wd_moe_set_plan(spec=None):
     """Override the launch plan (see include/wd_moe.h); None restores the default."""
     _check("wd_moe_set_plan", lib().wd_moe_set_plan(None if spec is None else spec.encode()))
+
+
+def wd_last_error_string() -> str:
+    """Name of the CUDA error behind this thread's last WD_ERR_CUDA ("none" if none)."""
+    return lib().wd_last_error_string().decode()
 
 
 def wd_moe_describe_plan(B, H, I, E, K) -> str:

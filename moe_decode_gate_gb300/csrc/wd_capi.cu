@@ -22,7 +22,7 @@ namespace wd {
 // wd_moe_set_plan (or the WD_PLAN environment variable, read at the first
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
-//   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<sbw>",
+//   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma",
 //   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>",
 //   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
 namespace {
@@ -54,6 +54,14 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpStream;
         p.gu_npw = a;
         p.gu_cpl = b;
+      } else if (strcmp(tok, "gu=tma") == 0) {
+        p.gu_variant = kGateUpTma;
+        p.gu_npw = 2;
+        p.gu_cpl = 3;
+      } else if (sscanf(tok, "gu=ring:%d", &a) == 1) {
+        p.gu_variant = kGateUpRing;
+        p.gu_npw = a;
+        p.gu_cpl = 0;
       } else if (sscanf(tok, "gu=persist:%d:%d", &a, &b) == 2) {
         p.gu_variant = kGateUpPersist;
         p.gu_npw = a;
@@ -108,6 +116,10 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
   if (o.gu_variant == kGateUpRowShare && rowshare_ok) return {kGateUpRowShare, o.gu_npw, o.gu_cpl};
   if (o.gu_variant == kGateUpPersist && gate_up_persist_supported(B, H, I, E, K))
     return {kGateUpPersist, o.gu_npw, o.gu_cpl};
+  if (o.gu_variant == kGateUpRing && gate_up_ring_supported(B, H, I, E, K, o.gu_npw))
+    return {kGateUpRing, o.gu_npw, 0};
+  if (o.gu_variant == kGateUpTma && gate_up_tma_supported(B, H, I, E, K))
+    return {kGateUpTma, 2, 3};
   if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
   // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack
   // (H=2048, I=768, E=128, K=8): one warp per (token, slot, neuron group) while
@@ -140,9 +152,11 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
   GateUpPlan p = plan_gate_up(a.B, a.H, a.I, a.K, a.E);
-  if ((p.variant == kGateUpStream || p.variant == kGateUpMixed) &&
+  if ((p.variant == kGateUpStream || p.variant == kGateUpMixed || p.variant == kGateUpRing ||
+       p.variant == kGateUpTma) &&
       !(aligned16(a.gate_up) && aligned16(a.gate_up_scale)))
-    p = {kGateUpBatched, 2, 1};
+    p = gate_up_persist_supported(a.B, a.H, a.I, a.E, a.K) ? GateUpPlan{kGateUpPersist, 2, 1}
+                                                           : GateUpPlan{kGateUpBatched, 2, 1};
   return p;
 }
 
@@ -176,9 +190,14 @@ wd_status check_dims(int B, int H, int I, int E, int K) {
   return WD_OK;
 }
 
+// Name of the CUDA error behind this thread's last WD_ERR_CUDA.
+thread_local const char* g_last_cuda_error = "none";
+
 wd_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) e = cudaGetLastError();
-  return e == cudaSuccess ? WD_OK : WD_ERR_CUDA;
+  if (e == cudaSuccess) return WD_OK;
+  g_last_cuda_error = cudaGetErrorName(e);
+  return WD_ERR_CUDA;
 }
 
 }  // namespace
@@ -284,6 +303,8 @@ wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_str
 
 int wd_moe_launches_per_call(void) { return 2; }
 
+const char* wd_last_error_string(void) { return g_last_cuda_error; }
+
 wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, size_t bytes) {
   if (!buf || bytes < 128) return WD_ERR_INVALID_ARG;
   const wd_status st = check_dims(B, H, I, E, K);
@@ -292,10 +313,11 @@ wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, siz
   const wd::DownPlan d = wd::plan_down(B, H, I, K, E);
   static const char* const gu_names[] = {"moe_gate_up_3d_batched", "moe_gate_up_rowshare",
                                          "moe_gate_up_stream", "moe_gate_up_mixed",
-                                         "moe_gate_up_persist"};
+                                         "moe_gate_up_persist", "moe_gate_up_ring",
+                                         "moe_gate_up_tma"};
   static const char* const dn_names[] = {"moe_down_3d_batched", "moe_down_stream",
                                          "moe_down_3d_batched_persist", "moe_down_shared"};
-  const char* gn = (g.variant >= 0 && g.variant <= 4) ? gu_names[g.variant] : "?";
+  const char* gn = (g.variant >= 0 && g.variant <= 6) ? gu_names[g.variant] : "?";
   const char* dn = (d.variant >= 0 && d.variant <= 3) ? dn_names[d.variant] : "?";
   snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d>", gn, g.npw, g.cpl, dn, d.rpw, d.qpl);
   return WD_OK;

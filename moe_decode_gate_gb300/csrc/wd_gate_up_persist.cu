@@ -19,80 +19,33 @@
 //     tokens cost T + kItemBase units), so experts with many tokens do not
 //     leave a tail;
 //   - when a CTA moves to a new expert it stages that expert's tokens' x rows
-//     in shared memory once, converted to FP32, in a layout whose 16-byte
-//     chunks are XOR-swizzled by block so that the lanes of a warp (one MXFP8
-//     block each) read them without bank conflicts.  The dot products then
-//     read activations from shared memory with no conversion;
+//     in shared memory once, converted to FP32, each 32-element block padded
+//     to 144 bytes so that the lanes of a warp (one MXFP8 block each) read them
+//     without bank conflicts at immediate offsets.  The dot products then read
+//     activations from shared memory with no conversion;
 //   - the E8M0 block scale multiplies each 32-element partial sum rather than
 //     every element (exact for a power of two barring FP32 over/underflow);
 //   - the 4*TC partial sums of a chunk of TC tokens are reduced across the
 //     warp by a transpose-reduction (each shuffle step halves the number of
 //     values per lane), after which lane pairs hold gate and up of one output.
-#include "wd_device.cuh"
 #include "wd_launch.h"
-#include "wd_pipeline.cuh"
-#include "wd_routing.cuh"
+#include "wd_persist.cuh"
 
 namespace wd {
 
 namespace {
 
-constexpr int kPWarps = 8;
-constexpr int kPThreads = 32 * kPWarps;
 constexpr int kItemBase = 3;                   // item cost = T + kItemBase
 constexpr int kXMaxTokens = 8;                 // x rows staged at once (upper bound)
 constexpr int kXBudget = 96 * 1024;            // shared-memory bytes for staged x
 
 __host__ __device__ inline int persist_x_tokens(int H) {
-  const int t = kXBudget / (H * 4);
+  const int t = kXBudget / x_padded_row_bytes(H);
   return t < 1 ? 1 : (t > kXMaxTokens ? kXMaxTokens : t);
 }
 
-// Staged x starts on a 128-byte boundary after the routing tables (its
-// 16-byte vector accesses need at least 16-byte alignment).
-constexpr int kXOffset = (routing_table_bytes() + 127) / 128 * 128;
-static_assert(kXOffset % 16 == 0 && kXOffset >= routing_table_bytes(), "staged x alignment");
-
 __host__ __device__ inline int persist_smem_bytes(int H) {
-  return kXOffset + persist_x_tokens(H) * H * 4;
-}
-
-// Shared-memory byte offset of 16-byte chunk c (elements 4c..4c+3) of MXFP8
-// block `blk` of staged token t.
-__device__ __forceinline__ uint32_t xs_chunk(uint32_t xs, int t, int H, int blk, int c) {
-  return xs + (uint32_t)(t * H + blk * 32) * 4u + (uint32_t)((c ^ (blk & 7)) << 4);
-}
-
-__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-// Sum over the warp of V values per lane (V a power of two, 2..16), by
-// transpose-reduction: lane l ends with the sum of value index l >> (5 - log2 V).
-template <int V>
-__device__ __forceinline__ float transpose_reduce(float (&v)[V]) {
-  constexpr int L = V == 2 ? 1 : (V == 4 ? 2 : (V == 8 ? 3 : 4));
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int k = 0; k < L; ++k) {
-    const int off = 16 >> k;
-    const int n = V >> k;
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
-    }
-  }
-  float s = v[0];
-#pragma unroll
-  for (int off = 16 >> L; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-  return s;
+  return kXOffset + persist_x_tokens(H) * x_padded_row_bytes(H);
 }
 
 // One chunk of TC (<= 4) tokens for this warp's NPW neurons: dots of its
@@ -112,6 +65,7 @@ __device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_u
   const uint8_t* sbase = gate_up_scale + gate_row0 * nblk;
   const size_t wup = (size_t)I * H;
   const int sup = I * nblk;
+  const int row_bytes = x_padded_row_bytes(H);
   float acc[TCP][R];
 #pragma unroll
   for (int t = 0; t < TCP; ++t)
@@ -131,17 +85,19 @@ __device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_u
     for (int t = 0; t < TC; ++t)
 #pragma unroll
       for (int r = 0; r < R; ++r) p[t][r] = make_float2(0.f, 0.f);
-    const uint32_t xb = xs + (uint32_t)(t0 * H + blk * 32) * 4u;
-    const int sw = blk & 7;
+    // padded x layout: chunk c of this lane's block is at xt[t] + 16 c
+    uint32_t xt[TC];
+#pragma unroll
+    for (int t = 0; t < TC; ++t)
+      xt[t] = xs + (uint32_t)((t0 + t) * row_bytes + blk * kXPadBlockBytes);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       float2 wf[R][2];
 #pragma unroll
       for (int r = 0; r < R; ++r) e4m3x4_to_f32(wv[r].v[c], wf[r][0], wf[r][1]);
-      const uint32_t xc = xb + (uint32_t)((c ^ sw) << 4);
 #pragma unroll
       for (int t = 0; t < TC; ++t) {
-        const float4 xv = lds_f32x4(xc + (uint32_t)(t * H * 4));
+        const float4 xv = lds_f32x4(xt[t] + 16 * c);
         const float2 x01 = make_float2(xv.x, xv.y), x23 = make_float2(xv.z, xv.w);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -156,21 +112,7 @@ __device__ __forceinline__ void persist_chunk(const uint8_t* __restrict__ gate_u
       for (int r = 0; r < R; ++r) acc[t][r] = fmaf(p[t][r].x + p[t][r].y, sc[r], acc[t][r]);
   }
 
-  // value index t*R + r; after the reduction lane l holds index l >> (5 - L),
-  // and index bit log2(NPW) (gate/up) sits at lane bit 5 - L + log2(NPW)
-  constexpr int V = R * TCP;
-  constexpr int L = V == 2 ? 1 : (V == 4 ? 2 : (V == 8 ? 3 : 4));
-  float v[V];
-#pragma unroll
-  for (int t = 0; t < TCP; ++t)
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[t * R + r] = acc[t][r];
-  const float s = transpose_reduce<V>(v);
-  const float up = __shfl_xor_sync(0xFFFFFFFFu, s, NPW << (5 - L));
-  const int idx = lane >> (5 - L);
-  const int t = idx / R, r = idx % R;
-  if ((lane & ((1 << (5 - L)) - 1)) == 0 && r < NPW && t < TC)
-    h[(size_t)slots[t] * I + n0 + r] = __float2bfloat16_rn(silu(s) * up);
+  store_chunk<NPW, TC, TCP>(acc, h, slots, n0, I);
 }
 
 }  // namespace
@@ -196,50 +138,21 @@ __global__ void __launch_bounds__(kPThreads, MINB) moe_gate_up_persist(
   grid_launch_dependents();
   build_routing_tables(rt, topk_ids, BK, E, 4, kPThreads);
 
-  // out-of-range ids: CTA 0 zeroes their h rows and raises the flag
-  if (rt.scalar[2] && blockIdx.x == 0) {
-    for (int s = 0; s < BK; ++s) {
-      const int e = rt.ids[s];
-      if (e < 0 || e >= E)
-        for (int n = tid; n < I; n += kPThreads) h[(size_t)s * I + n] = __float2bfloat16_rn(0.0f);
-    }
-    if (tid == 0 && error_flag) atomicOr(error_flag, 1u);
-  }
+  zero_bad_slots(rt, h, error_flag, BK, I, E);
 
-  // cost prefix over routed experts: item of expert u costs T_u + kItemBase,
-  // and expert u has nb items.  `coff` ([S + 1], unused here) holds the prefix.
+  // cost-balanced contiguous range of (expert, neuron block) items for this CTA;
+  // `coff` ([S + 1], unused here) holds the cost prefix
   const int U = rt.scalar[0];
   constexpr int kNeurons = kPWarps * NPW;  // neurons per item
   const int nb = (I + kNeurons - 1) / kNeurons;
-  int* pc = rt.coff;  // [U + 1]
-  if (warp == 0) {
-    int base = 0;
-    for (int u0 = 0; u0 < U; u0 += 32) {
-      const int u = u0 + lane;
-      const int c = u < U ? nb * (rt.off[u + 1] - rt.off[u] + kItemBase) : 0;
-      int excl, total;
-      warp_exclusive_scan(c, excl, total);
-      if (u < U) pc[u] = base + excl;
-      base += total;
-    }
-    if (lane == 0) pc[U] = base;
-  }
-  __syncthreads();
+  int* pc = rt.coff;
+  expert_cost_prefix(rt, nb, kItemBase, pc);
   const long long total = pc[U];
   const int lo = (int)(total * blockIdx.x / gridDim.x);
   const int hi = (int)(total * (blockIdx.x + 1) / gridDim.x);
   if (lo >= hi) return;
 
-  // first expert whose cost range reaches lo
-  int u = 0;
-  {
-    int a = 0, b = U - 1;
-    while (a < b) {  // largest u with pc[u] <= lo
-      const int m = (a + b + 1) >> 1;
-      if (pc[m] <= lo) a = m; else b = m - 1;
-    }
-    u = a;
-  }
+  int u = first_expert(pc, U, lo);
   const uint8_t* xg = reinterpret_cast<const uint8_t*>(x) + wait_token;
   for (; u < U && pc[u] < hi; ++u) {
     const int T = rt.off[u + 1] - rt.off[u];
@@ -252,21 +165,7 @@ __global__ void __launch_bounds__(kPThreads, MINB) moe_gate_up_persist(
     const size_t expert_row0 = (size_t)rt.expert[u] * 2 * I;
     for (int q0 = 0; q0 < T; q0 += xtok) {
       const int nq = min(xtok, T - q0);
-      // stage x of tokens q0..q0+nq-1 as FP32, swizzled (all warps)
-      __syncthreads();  // the previous group's x is no longer read
-      const int units = nq * (H >> 2);  // 16-byte FP32 chunks
-      for (int i = tid; i < units; i += kPThreads) {
-        const int t = i / (H >> 2);
-        const int k = i - t * (H >> 2);  // chunk index within the row: block k>>3, chunk k&7
-        const int b = slots[q0 + t] / K;
-        const uint2 raw = *reinterpret_cast<const uint2*>(xg + ((size_t)b * H + (size_t)k * 4) * 2);
-        const float2 lo2 = bf16x2_to_f32(raw.x), hi2 = bf16x2_to_f32(raw.y);
-        const uint32_t a = xs_chunk(xs, t, H, k >> 3, k & 7);
-        asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(lo2.x), "f"(lo2.y),
-                     "f"(hi2.x), "f"(hi2.y)
-                     : "memory");
-      }
-      __syncthreads();
+      stage_x_padded(xs, xg, slots + q0, nq, H, K);
       // this warp's rows (NPW gate, NPW up; each group contiguous) of item gp, into L2
       auto prefetch_item = [&](int gp) {
         const int np = (gp * kPWarps + warp) * NPW;

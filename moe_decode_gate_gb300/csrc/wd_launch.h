@@ -39,6 +39,8 @@ enum GateUpVariant {
   kGateUpStream = 2,    // moe_gate_up_stream: rows streamed by bulk copies through shared memory
   kGateUpMixed = 3,     // moe_gate_up_mixed: streamed rows, FP16 x FP16 -> FP32 products
   kGateUpPersist = 4,   // moe_gate_up_persist: one wave of CTAs over shared expert rows, x staged
+  kGateUpRing = 5,      // moe_gate_up_ring: as persist, rows through a per-warp bulk-copy ring
+  kGateUpTma = 6,       // moe_gate_up_tma: as persist, rows by 2-D TMA into a CTA-wide ring
 };
 
 // Compile-time shape of one kernel instance.
@@ -79,6 +81,12 @@ bool gate_up_mixed_supported(int B, int H, int I, int E, int K, int npw);
 cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                    bool pdl);
 bool gate_up_persist_supported(int B, int H, int I, int E, int K);
+cudaError_t launch_gate_up_ring(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                                bool pdl);
+bool gate_up_ring_supported(int B, int H, int I, int E, int K, int stages);
+cudaError_t launch_gate_up_tma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                               bool pdl);
+bool gate_up_tma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_stream_supported(int B, int H, int I, int E, int K);

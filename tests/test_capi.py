@@ -124,6 +124,10 @@ def test_bench_kernels_reject_unaligned_buffers():
     assert lib.wd_bench_fill(None, 1024, 0, 0, None) == einval
 
 
+def test_last_error_string_starts_empty():
+    assert wd.wd_last_error_string() == "none"
+
+
 def test_launch_count():
     assert wd.wd_moe_launches_per_call() == 2
 
@@ -162,6 +166,8 @@ def test_plan_override_parser():
     assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
     assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=persist:4:1") == OK
     assert lib.wd_moe_set_plan(b"gu=persist:1:1,dn=shared:2") == OK
+    assert lib.wd_moe_set_plan(b"gu=tma,dn=4:1") == OK
+    assert lib.wd_moe_set_plan(b"gu=ring:2") == OK
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID
     assert lib.wd_moe_set_plan(None) == OK

@@ -242,6 +242,9 @@ PLANS = [
     "gu=persist:1:2,dn=4:1",
     "gu=persist:2:2,dn=persist:1:6",
     "gu=persist:2:2,dn=shared:4",
+    "gu=ring:2,dn=4:1",
+    "gu=ring:3,dn=2:3",
+    "gu=tma,dn=4:1",
     "gu=batched:2:1,dn=shared:2",
 ]
 
@@ -256,6 +259,7 @@ PLAN_SHAPES = [
     (9, 512, 128, 8, 3, "uniform"),       # smallest shape both streamed kernels accept
     (17, 1024, 832, 20, 5, "uniform"),    # I = 832: ragged lane slices in both
     (12, 8192, 64, 3, 2, "uniform"),      # H = 8192: x of 3 tokens staged at a time, ~8 per expert
+    (20, 1024, 96, 6, 4, "uniform"),      # smallest H the bulk-copy ring accepts, ~13 tokens per expert
 ]
 
 
@@ -280,7 +284,9 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
 @pytest.mark.parametrize("plan", ["gu=rowshare:2:2,rowshare_min_b=1,dn=2:3",
                                   "gu=stream:2:3,dn=stream:8",
                                   "gu=persist:2:2,dn=persist:4:1",
-                                  "gu=persist:2:2,dn=shared:4"])
+                                  "gu=persist:2:2,dn=shared:4",
+                                  "gu=ring:2,dn=4:1",
+                                  "gu=tma,dn=4:1"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
