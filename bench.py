@@ -427,6 +427,37 @@ def config_dict(B):
             "parallelism": "replicas"}
 
 
+class RankOps:
+    """Reductions over the bench's ranks (one process per GPU, replicas): a
+    barrier, the max of a per-rank time and the sum of per-rank bytes.  With
+    no process group (one GPU) they return the local value."""
+
+    def __init__(self, torch, dist, device):
+        self.torch, self.dist, self.device = torch, dist, device
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def _reduce(self, v, op):
+        if self.dist is None:
+            return v
+        t = self.torch.tensor([v], dtype=self.torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    def max(self, v):
+        return self._reduce(v, None if self.dist is None else self.dist.ReduceOp.MAX)
+
+    def sum(self, v):
+        return self._reduce(v, None if self.dist is None else self.dist.ReduceOp.SUM)
+
+
+def aggregate_gbps(local_bytes, local_ms, ranks):
+    """Whole-job GB/s of N replicas: all ranks' bytes over the slowest rank's time."""
+    return ranks.sum(float(local_bytes)) / ranks.max(local_ms) / 1e6
+
+
 # ------------------------------------------------------------------- main --
 
 def main():
@@ -469,23 +500,8 @@ def main():
 
         dist.init_process_group("nccl", device_id=dev)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+    ranks = RankOps(torch, dist, dev)
+    barrier, max_over_ranks, sum_over_ranks = ranks.barrier, ranks.max, ranks.sum
 
     peaks_file, peaks_kind = read_peaks_file()
     if args.quick:  # profiling runs keep the device footprint small
@@ -525,7 +541,7 @@ def main():
         ms_local = time_graph(torch, dev, g, s, args.steps, args.warmup, barrier)
     ms = max_over_ranks(ms_local)
     total_bytes = sum_over_ranks(float(nb))
-    value = total_bytes / ms / 1e6  # GB/s over all ranks (bytes / max time)
+    value = aggregate_gbps(nb, ms_local, ranks)  # all ranks' bytes / the slowest rank's time
     per_rank_gbs = nb / ms / 1e6
     sweep_rows.append({"B": B, "us_per_layer": round(ms * 1e3 / stack.L, 2),
                        "GBps": round(per_rank_gbs, 1),
