@@ -143,13 +143,18 @@ WD_API int wd_moe_launches_per_call(void);
  *   "gu=batched:<neurons per warp>:<blocks per lane per pass>"
  *   "gu=rowshare:<neurons per warp>:<words per step>"   (tokens share rows)
  *   "gu=persist:<neurons per warp>:<1 + L2 prefetch distance>"
- *   "gu=ring:<bulk-copy ring stages per warp>" | "gu=tma"
+ *   "gu=ring:<bulk-copy ring stages per warp>" | "gu=tma" |
+ *   "gu=mma[:<ring stages, 2..4>]"  (tensor-core products; B*K <= 256,
+ *                                    H % 512 == 0, H <= 2048, I % 16 == 0)
  *   "gu=stream:<variant>:<stages>" | "gu=mixed:<variant>:<stages>"
  *   "dn=<output dims per warp>:<blocks per lane per pass>"
  *   "dn=persist:<output dims per warp>:<blocks per lane per pass>"
  *   "dn=stream:<stages>" | "dn=shared:<output dims per CTA>"
  *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel
  *                    where the persistent one does not apply>"
+ *   "pdl=<0..3>" (programmatic dependent launch: bit 0 lets the gate/up
+ *                 launch overlap the kernel before it, bit 1 lets the down
+ *                 launch overlap gate/up)
  * NULL or "" restores the built-in plan.  Returns WD_ERR_INVALID_ARG for an
  * unparsable spec (the plan is then unchanged); a variant that does not
  * support the call's shape falls back to the built-in choice, and an
@@ -161,7 +166,8 @@ WD_API wd_status wd_moe_set_plan(const char* spec);
 
 /* Write the kernels wd_moe_decode would launch for this shape under the
  * current plan (16-byte-aligned weight pointers assumed), as
- * "gate_up=<kernel><params> down=<kernel><params>", NUL-terminated, into
+ * "gate_up=<kernel><params> down=<kernel><params> pdl=<mask>" (the mask as in
+ * wd_moe_set_plan's "pdl="), NUL-terminated, into
  * `buf` (`bytes` long; 128 bytes always suffice).  Host-only: launches
  * nothing.  Returns WD_ERR_INVALID_ARG for a NULL or too small buffer and the
  * status wd_moe_decode would return for invalid dimensions. */

@@ -22,15 +22,19 @@ namespace wd {
 // wd_moe_set_plan (or the WD_PLAN environment variable, read at the first
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
-//   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma",
+//   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma" |
+//   "gu=mma[:<stages>]",
 //   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>",
-//   "rowshare_min_b=<B>", comma-separated; "" or NULL restores the defaults.
+//   "rowshare_min_b=<B>", "pdl=<mask>" (bit 0: the gate/up launch may overlap the
+//   kernel before it, bit 1: the down launch may overlap gate/up), comma-separated;
+//   "" or NULL restores the defaults.
 namespace {
 
 struct PlanOverride {
   int gu_variant = -1, gu_npw = 0, gu_cpl = 0;
   int dn_variant = -1, dn_rpw = 0, dn_qpl = 0;
   int rowshare_min_b = 16;  // shared-row kernel where the persistent one does not apply
+  int pdl_mask = -1;        // -1: by the plan (pdl_mask_for)
 };
 
 bool parse_plan(const char* spec, PlanOverride* out) {
@@ -54,6 +58,14 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpStream;
         p.gu_npw = a;
         p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=mma:%d", &a) == 1) {
+        p.gu_variant = kGateUpMma;
+        p.gu_npw = 8;
+        p.gu_cpl = a;
+      } else if (strcmp(tok, "gu=mma") == 0) {
+        p.gu_variant = kGateUpMma;
+        p.gu_npw = 8;
+        p.gu_cpl = 0;
       } else if (strcmp(tok, "gu=tma") == 0) {
         p.gu_variant = kGateUpTma;
         p.gu_npw = 2;
@@ -86,6 +98,8 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.dn_qpl = b;
       } else if (sscanf(tok, "rowshare_min_b=%d", &a) == 1) {
         p.rowshare_min_b = a;
+      } else if (sscanf(tok, "pdl=%d", &a) == 1 && a >= 0 && a <= 3) {
+        p.pdl_mask = a;
       } else {
         return false;
       }
@@ -120,11 +134,15 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
     return {kGateUpRing, o.gu_npw, 0};
   if (o.gu_variant == kGateUpTma && gate_up_tma_supported(B, H, I, E, K))
     return {kGateUpTma, 2, 3};
+  if (o.gu_variant == kGateUpMma && gate_up_mma_supported(B, H, I, E, K))
+    return {kGateUpMma, 8, o.gu_cpl};
   if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
   // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack
   // (H=2048, I=768, E=128, K=8): one warp per (token, slot, neuron group) while
-  // tokens rarely share experts (2*B*K < E); one wave of persistent CTAs, each
-  // expert row dequantised once for all its tokens, once they do.
+  // tokens rarely share experts (2*B*K < E); once they do, one wave of
+  // persistent CTAs that read each expert row once for all its tokens, with
+  // the products on tensor cores where the shape allows.
+  if (2 * B * K >= E && gate_up_mma_supported(B, H, I, E, K)) return {kGateUpMma, 8, 0};
   if (2 * B * K >= E && gate_up_persist_supported(B, H, I, E, K)) return {kGateUpPersist, 2, 1};
   if (rowshare_ok && B >= o.rowshare_min_b) return {kGateUpRowShare, 2, 2};
   if (B == 1) return {kGateUpBatched, 1, 1};
@@ -148,12 +166,22 @@ DownPlan plan_down(int B, int H, int I, int K, int E) {
   return DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
 }
 
+// Programmatic dependent launch for the two launches of one call (bit 0:
+// gate/up after whatever precedes it on the stream, bit 1: down after gate/up).
+int pdl_mask_for(const GateUpPlan& g) {
+  const PlanOverride& o = plan_override();
+  if (o.pdl_mask >= 0) return o.pdl_mask;
+  // measured: letting the down kernel's CTAs start early while the one-CTA-per-SM
+  // tensor-core gate/up kernel runs costs 7-14% of the layer at B = 8..32
+  return g.variant == kGateUpMma ? 1 : 3;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
   GateUpPlan p = plan_gate_up(a.B, a.H, a.I, a.K, a.E);
   if ((p.variant == kGateUpStream || p.variant == kGateUpMixed || p.variant == kGateUpRing ||
-       p.variant == kGateUpTma) &&
+       p.variant == kGateUpTma || p.variant == kGateUpMma) &&
       !(aligned16(a.gate_up) && aligned16(a.gate_up_scale)))
     p = gate_up_persist_supported(a.B, a.H, a.I, a.E, a.K) ? GateUpPlan{kGateUpPersist, 2, 1}
                                                            : GateUpPlan{kGateUpBatched, 2, 1};
@@ -280,10 +308,12 @@ wd_status wd_moe_decode(const void* x, const int32_t* topk_ids, const float* top
   uint32_t* flag = flag_of(workspace);
   void* h = h_of(workspace);
   const wd::GateUpArgs ga{x, topk_ids, gate_up, gate_up_scale, h, flag, B, H, I, E, K};
-  st = cuda_status(wd::launch_gate_up(ga, wd::plan_gate_up_for(ga), s, true));
+  const wd::GateUpPlan gp = wd::plan_gate_up_for(ga);
+  const int pdl = wd::pdl_mask_for(gp);
+  st = cuda_status(wd::launch_gate_up(ga, gp, s, (pdl & 1) != 0));
   if (st != WD_OK) return st;
   const wd::DownArgs da{h, topk_ids, topk_w, down, down_scale, out, flag, B, H, I, E, K};
-  return cuda_status(wd::launch_down(da, wd::plan_down_for(da), s, true));
+  return cuda_status(wd::launch_down(da, wd::plan_down_for(da), s, (pdl & 2) != 0));
 }
 
 wd_status wd_moe_read_error_flag(void* workspace, size_t workspace_bytes, wd_stream_t stream,
@@ -314,12 +344,13 @@ wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, siz
   static const char* const gu_names[] = {"moe_gate_up_3d_batched", "moe_gate_up_rowshare",
                                          "moe_gate_up_stream", "moe_gate_up_mixed",
                                          "moe_gate_up_persist", "moe_gate_up_ring",
-                                         "moe_gate_up_tma"};
+                                         "moe_gate_up_tma", "moe_gate_up_mma"};
   static const char* const dn_names[] = {"moe_down_3d_batched", "moe_down_stream",
                                          "moe_down_3d_batched_persist", "moe_down_shared"};
-  const char* gn = (g.variant >= 0 && g.variant <= 6) ? gu_names[g.variant] : "?";
+  const char* gn = (g.variant >= 0 && g.variant <= 7) ? gu_names[g.variant] : "?";
   const char* dn = (d.variant >= 0 && d.variant <= 3) ? dn_names[d.variant] : "?";
-  snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d>", gn, g.npw, g.cpl, dn, d.rpw, d.qpl);
+  snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d> pdl=%d", gn, g.npw, g.cpl, dn, d.rpw,
+           d.qpl, wd::pdl_mask_for(g));
   return WD_OK;
 }
 

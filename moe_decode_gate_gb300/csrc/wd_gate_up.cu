@@ -135,6 +135,7 @@ cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_
   if (p.variant == kGateUpPersist) return launch_gate_up_persist(a, p, stream, pdl);
   if (p.variant == kGateUpRing) return launch_gate_up_ring(a, p, stream, pdl);
   if (p.variant == kGateUpTma) return launch_gate_up_tma(a, p, stream, pdl);
+  if (p.variant == kGateUpMma) return launch_gate_up_mma(a, p, stream, pdl);
 #define WD_GU_CASE(NPW, CPL) \
   if (p.npw == NPW && p.cpl == CPL) return launch_gate_up_t<NPW, CPL>(a, stream, pdl);
   WD_GU_CASE(1, 1)

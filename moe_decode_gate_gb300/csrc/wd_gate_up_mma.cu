@@ -1,0 +1,580 @@
+// wd_gate_up_mma.cu - moe_gate_up_mma: the gate/up kernel for batches whose
+// tokens share experts, with the multiply-accumulate of the dequantised rows
+// and the activations done by warp-level tensor-core MMAs.
+//
+// Computes what moe_gate_up_3d_batched computes (Cursor, "用 warp decode 实现
+// 更好的 MoE 模型推理", section 两个 kernel 如何工作, gate/up paragraph): for
+// every (token, routed slot) and intermediate neuron n, the dot products of
+// gate row n and up row I+n of the routed expert with x, then one BF16 value
+// bf16(SiLU(g) * u), written once, with no padding, scatter or combine pass.
+//
+// Why tensor cores here.  Once the tokens routed to one expert are grouped
+// (as moe_gate_up_persist does), the work of that expert is a small dense
+// product [2I x H] . [H x T] with T tokens.  On CUDA cores the dequantisation
+// (E4M3 -> FP16 -> FP32) and the T FP32 multiply-adds per weight cost ~4.8
+// warp instructions per weight element at B = 32, which bounds that kernel by
+// instruction issue, not by HBM.  Here each weight element costs one half of a
+// cvt (E4M3x2 -> F16x2, exact) and its share of one mma.sync.m16n8k16 per 256
+// elements, whatever T is (up to 8 tokens per MMA column tile).
+//
+// Organisation:
+//   - an item is (routed expert, 16 neurons): gate rows n0..n0+15 and up rows
+//     I+n0..I+n0+15, computed as two 16-row MMA tiles; tile r has gate rows
+//     n0+8r..n0+8r+7 as rows 0..7 and the matching up rows as rows 8..15, so
+//     the lane holding gate(n, t) in the accumulator also holds up(n, t);
+//   - one CTA per SM walks a contiguous, cost-balanced range of items (after
+//     building the routing tables once).  A producer thread streams each item
+//     into an S-stage shared-memory ring with four copies that complete on the
+//     stage's mbarrier: the 16 gate rows and the 16 up rows (each one 3-D
+//     tensor-map copy, 16 x H bytes, 128-byte swizzled so that the MMA fragment
+//     reads of 8 rows hit different banks) and their scale bytes (two bulk
+//     copies of 16 x H/32 bytes).  The bytes in flight are held by shared
+//     memory (two items, 130 KiB per SM at H = 2048), not by registers;
+//   - 8 consumer warps split H: warp w owns the 256-column chunks w, w+8, ...
+//     of the item.  Their partial accumulators are summed through shared
+//     memory (one named barrier per item); the epilogue is lane-local;
+//   - MXFP8 block scales: the two k16 MMAs of one 32-column block accumulate
+//     into a fresh tile, which is then multiplied by the block's power-of-two
+//     scale into the running FP32 sum (exact barring FP32 over/underflow);
+//   - the k index inside a block is permuted (lane quad tig takes columns
+//     8 tig .. 8 tig + 7, i.e. 8 contiguous bytes of each of its rows), and
+//     the activations are staged with the same permutation, which for this
+//     fragment layout is the natural column order;
+//   - activations: when the CTA enters an expert its consumer warps stage the
+//     x rows of its tokens (up to 8 at a time) in shared memory as FP16, each
+//     token scaled by a power of two 2^k_t so that its largest magnitude falls
+//     in [2^14, 2^15).  Power-of-two scaling is exact, and every BF16 value
+//     within 2^31 of the token's largest magnitude is an FP16 value after it,
+//     so the re-encoding is exact for those; smaller values are rounded to a
+//     grid of 2^-38 of that largest magnitude, below the rounding of the FP32
+//     accumulation itself.  The accumulators are multiplied by 2^-k_t in the
+//     epilogue.  FP16 x FP16 products are exact in FP32; the MMA accumulates in
+//     FP32.  An expert with more than 8 tokens is computed in groups of 8,
+//     each reading the item's rows again (from L2).
+//
+// Every mbarrier wait is bounded (wd_pipeline.cuh).  A consumer whose wait
+// runs out raises bit 1 of the error flag and computes nothing more but keeps
+// following the consumers' barriers; the producer stops issuing when its wait
+// runs out, and before exiting waits (bounded) for the copies it issued last.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "wd_launch.h"
+#include "wd_persist.cuh"
+
+namespace wd {
+
+namespace {
+
+constexpr int kMWarps = 8;                 // consumer warps
+constexpr int kMThreads = 32 * kMWarps;
+constexpr int kMTokens = 8;                // tokens staged at once: one MMA column tile
+constexpr int kMNeurons = 16;              // neurons per item: two 16-row MMA tiles
+constexpr int kMItemBase = 8;              // item cost = groups * kMItemBase + 1
+constexpr int kMRedBytes = 2 * kMWarps * 2 * 32 * 16;  // [2 parities][warps][2 tiles][32] float4
+constexpr int kMScaleBytes = kMWarps * 1024;          // per-warp FP32 tables [32 rows][8 blocks]
+constexpr int kMSmemCap = 227 * 1024;
+constexpr int kMMaxStages = 4;
+
+__host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Shared-memory layout for a given H and ring depth S.  A stage holds the
+// gate slab (16 rows, as [H/128][16][128] swizzled bytes), the up slab (same),
+// then the 16 gate rows' scale bytes and the 16 up rows' (16 * H/32 each).
+struct MmaLayout {
+  int slab;     // bytes of one slab (16 * H)
+  int stage;    // bytes of one stage, a multiple of 1024
+  int bars;     // full[kMMaxStages], then empty[kMMaxStages] (8 bytes each)
+  int ring;     // S stages, 1024-byte aligned
+  int xs;       // staged FP16 activations, `xtok` rows of `xstride` bytes
+  int xstride;
+  int xtok;
+  int ktok;     // per staged token exponent k_t (int[kMTokens])
+  int red;      // partial sums
+  int scl;      // per-warp scale tables
+  int total;
+};
+
+__host__ __device__ inline MmaLayout mma_layout(int H, int S) {
+  MmaLayout L;
+  L.slab = 16 * H;
+  L.stage = round_up(2 * L.slab + 2 * 16 * (H / 32), 1024);
+  L.bars = kXOffset;
+  L.ring = round_up(kXOffset + 16 * kMMaxStages, 1024);
+  L.xs = L.ring + S * L.stage;
+  // FP16 row rounded up to 128 bytes, plus 64, so that the two token rows
+  // read by one quarter-warp fall in different halves of the 32 banks
+  L.xstride = round_up(2 * H, 128) + 64;
+  const int fixed = L.xs + 64 + kMRedBytes + kMScaleBytes;
+  const int t = (kMSmemCap - fixed) / L.xstride;
+  L.xtok = t > kMTokens ? kMTokens : (t < 0 ? 0 : t);
+  L.ktok = L.xs + L.xtok * L.xstride;
+  L.red = L.ktok + 64;
+  L.scl = L.red + kMRedBytes;
+  L.total = L.scl + kMScaleBytes;
+  return L;
+}
+
+// Byte offset of (row, col) in a 128-byte-swizzled slab [H/128][16][128]:
+// 16-byte chunk q of a 128-byte line is stored at q ^ (row % 8).
+__device__ __forceinline__ uint32_t slab_offset(int row, int col) {
+  return (uint32_t)((col >> 7) * 2048 + row * 128 + ((((col & 127) >> 4) ^ (row & 7)) << 4) +
+                    (col & 15));
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// Bulk copy global -> shared without an L2 cache hint.
+__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Two E4M3 codes (low 16 bits of w) -> f16x2, element 0 in the low half (exact).
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
+}
+
+// d = A(16x16, f16) * B(16x8, f16), FP32 accumulate from zero.
+__device__ __forceinline__ void mma_f16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+// d += A * B.
+__device__ __forceinline__ void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+
+// 16 bytes of activations written by an earlier kernel: coherent load; `p`
+// must depend on grid_dependency_wait()'s token.
+__device__ __forceinline__ uint4 ld_act_16B(const void* p) {
+  uint4 r;
+  asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t w) {
+  return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+}
+
+// Exponent k such that 2^k times the largest magnitude (BF16 bits `mx`,
+// sign cleared) lies in [2^14, 2^15); 0 for an all-zero row or a row holding
+// Inf or NaN (whose results are not finite anyway).
+__device__ __forceinline__ int fp16_row_exponent(uint32_t mx) {
+  if (mx == 0u || mx >= 0x7F80u) return 0;
+  const int ef = (int)(mx >> 7);
+  const int e = ef ? ef - 127 : (31 - __clz((int)mx)) - 133;  // floor(log2(largest magnitude))
+  return 14 - e;
+}
+
+// 2^k for k in [-126, 127].
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
+
+// Stage the x rows of tokens slots[0..nq) (token b = slot / K) in shared
+// memory as FP16 scaled by 2^k_t, row t at xs + t * stride, and k_t in
+// ktok[t].  Warp w converts tokens w, w + 8, ...; no barrier.
+__device__ __forceinline__ void stage_x_f16(uint32_t xs, int stride, int* ktok, const uint8_t* xg,
+                                            const int* slots, int nq, int H, int K) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = H >> 3;  // 16-byte chunks of 8 BF16 values
+  for (int t = warp; t < nq; t += kMWarps) {
+    const uint8_t* row = xg + (size_t)(slots[t] / K) * H * 2;
+    uint32_t mx = 0u;
+    for (int i = lane; i < nch; i += 32) {
+      const uint4 v = ld_act_16B(row + i * 16);
+      mx = max(mx, max(max(max_abs_bf16x2(v.x), max_abs_bf16x2(v.y)),
+                       max(max_abs_bf16x2(v.z), max_abs_bf16x2(v.w))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    const int k = fp16_row_exponent(mx);
+    const int k1 = k >> 1, k2 = k - k1;  // each within [-57, 74]
+    const float f1 = exp2_int(k1), f2 = exp2_int(k2);
+    for (int i = lane; i < nch; i += 32) {
+      const uint4 v = ld_act_16B(row + i * 16);
+      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = bf16x2_to_f32(in[q]);
+        const __half2 hv = __floats2half2_rn((f.x * f1) * f2, (f.y * f1) * f2);
+        o[q] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xs + (uint32_t)(t * stride + i * 16)),
+                   "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                   : "memory");
+    }
+    if (lane == 0) ktok[t] = k;
+  }
+}
+
+__device__ __forceinline__ int mma_item_cost(int T, int xtok) {
+  return ((T + xtok - 1) / xtok) * (kMItemBase + 1);
+}
+
+// pc[u] = cost of the items of routed experts before u (nb items each); warp
+// 0 computes it, then a CTA barrier.
+__device__ __forceinline__ void mma_cost_prefix(const RoutingTables& rt, int nb, int xtok, int* pc) {
+  const int U = rt.scalar[0];
+  if ((threadIdx.x >> 5) == 0) {
+    const int lane = threadIdx.x & 31;
+    int acc = 0;
+    for (int u0 = 0; u0 < U; u0 += 32) {
+      const int u = u0 + lane;
+      const int c = u < U ? nb * mma_item_cost(rt.off[u + 1] - rt.off[u], xtok) : 0;
+      int excl, total;
+      warp_exclusive_scan(c, excl, total);
+      if (u < U) pc[u] = acc + excl;
+      acc += total;
+    }
+    if (lane == 0) pc[U] = acc;
+  }
+  __syncthreads();
+}
+
+// acc[r] += the contribution of 256-column chunk c of the item held in ring
+// stage `st`, for row tile r = 0, 1.  `xrow` is the shared-memory address of
+// this lane's staged activation row (token g of the group) at column 0 of the
+// chunk plus 16 * tig.  `scl` is this warp's 1 KiB table, into which the
+// chunk's 256 scale codes (32 rows x 8 blocks) are decoded first.
+__device__ __forceinline__ void mma_chunk(uint32_t st, int H, int c, float (&acc)[2][4],
+                                          uint32_t xrow, uint32_t scl) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  const int nblk = H >> 5;
+  const uint32_t gate = st, up = st + 16 * H, sc = st + 32 * H;
+  // lane l decodes table row l (gate rows 0..15, then up rows 0..15), blocks
+  // 8c .. 8c + 7
+  const uint2 codes = lds_u32x2(sc + lane * nblk + c * 8);
+  __syncwarp();  // the previous chunk's scale reads are done
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 32 * lane),
+               "f"(e8m0_to_f32(codes.x & 0xFFu)), "f"(e8m0_to_f32((codes.x >> 8) & 0xFFu)),
+               "f"(e8m0_to_f32((codes.x >> 16) & 0xFFu)), "f"(e8m0_to_f32(codes.x >> 24))
+               : "memory");
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 32 * lane + 16),
+               "f"(e8m0_to_f32(codes.y & 0xFFu)), "f"(e8m0_to_f32((codes.y >> 8) & 0xFFu)),
+               "f"(e8m0_to_f32((codes.y >> 16) & 0xFFu)), "f"(e8m0_to_f32(codes.y >> 24))
+               : "memory");
+  __syncwarp();
+  float4 sg4[2], su4[2];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if ((j & 3) == 0) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        sg4[r] = lds_f32x4(scl + 32 * (8 * r + g) + 4 * j);
+        su4[r] = lds_f32x4(scl + 32 * (16 + 8 * r + g) + 4 * j);
+      }
+    }
+    const uint4 b = lds_u32x4(xrow + 64 * j);
+    const int col = c * 256 + j * 32 + tig * 8;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float sg = (j & 3) == 0 ? sg4[r].x : (j & 3) == 1 ? sg4[r].y : (j & 3) == 2 ? sg4[r].z : sg4[r].w;
+      const float su = (j & 3) == 0 ? su4[r].x : (j & 3) == 1 ? su4[r].y : (j & 3) == 2 ? su4[r].z : su4[r].w;
+      const uint32_t off = slab_offset(8 * r + g, col);
+      const uint2 wg = lds_u32x2(gate + off), wu = lds_u32x2(up + off);
+      // columns 8 tig + 0..3 (first k16 step) and 8 tig + 4..7 (second)
+      const uint32_t a00 = e4m3x2_lo_to_f16x2(wg.x), a02 = e4m3x2_hi_to_f16x2(wg.x);
+      const uint32_t a01 = e4m3x2_lo_to_f16x2(wu.x), a03 = e4m3x2_hi_to_f16x2(wu.x);
+      const uint32_t a10 = e4m3x2_lo_to_f16x2(wg.y), a12 = e4m3x2_hi_to_f16x2(wg.y);
+      const uint32_t a11 = e4m3x2_lo_to_f16x2(wu.y), a13 = e4m3x2_hi_to_f16x2(wu.y);
+      float cc[4];
+      mma_f16_zero(cc, a00, a01, a02, a03, b.x, b.y);
+      mma_f16_acc(cc, a10, a11, a12, a13, b.z, b.w);
+      acc[r][0] = fmaf(cc[0], sg, acc[r][0]);
+      acc[r][1] = fmaf(cc[1], sg, acc[r][1]);
+      acc[r][2] = fmaf(cc[2], su, acc[r][2]);
+      acc[r][3] = fmaf(cc[3], su, acc[r][3]);
+    }
+  }
+}
+
+// Position in a CTA's walk: routed expert u, token group q (xtok tokens each),
+// item g in [g0, g1) (the items of u in this CTA's range).
+struct MmaCursor {
+  int u, q, g, g0, g1;
+};
+
+}  // namespace
+
+// Threads: kMWarps consumer warps, then one producer warp.  `S`: ring stages.
+// `tmap`: the gate/up codes as a 3-D byte tensor {128, E * 2I, H / 128} with
+// strides {H, 128}, boxes {128, 16, H / 128}, 128-byte swizzle.
+__global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
+    const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16* __restrict__ x,
+    const int32_t* __restrict__ topk_ids, const uint8_t* __restrict__ gate_up_scale,
+    __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I, int E,
+    int K, int S) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const RoutingTables rt = routing_tables_at(smem);
+  const MmaLayout L = mma_layout(H, S);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BK = B * K, nblk = H >> 5, nchunk = H >> 8;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t full = base + L.bars, empty = base + L.bars + 8 * kMMaxStages;
+  const uint32_t ring = base + L.ring;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + 8 * s, 1);
+      mbar_init(empty + 8 * s, kMWarps);
+    }
+    mbar_init_fence();
+  }
+  // x and topk_ids may come from the kernel before this one on the stream.
+  const uint32_t wait_token = grid_dependency_wait();
+  grid_launch_dependents();
+  build_routing_tables(rt, topk_ids, BK, E, 4, blockDim.x);  // ends with a CTA barrier
+  zero_bad_slots(rt, h, error_flag, BK, I, E);
+
+  // cost-balanced contiguous range of (expert, 16-neuron) items for this CTA
+  const int U = rt.scalar[0];
+  const int nb = I / kMNeurons;
+  const int xtok = L.xtok;
+  int* pc = rt.coff;
+  mma_cost_prefix(rt, nb, xtok, pc);
+  const int total = pc[U];
+  const int lo = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  if (lo >= hi) return;
+
+  // first item of routed expert u or later that lies in [lo, hi)
+  auto enter = [&](MmaCursor& c, int u) -> bool {
+    for (; u < U && pc[u] < hi; ++u) {
+      const int cu = mma_item_cost(rt.off[u + 1] - rt.off[u], xtok);
+      const int g0 = pc[u] >= lo ? 0 : (lo - pc[u] + cu - 1) / cu;
+      const int g1 = min(nb, (hi - pc[u] + cu - 1) / cu);
+      if (g0 < g1) {
+        c = MmaCursor{u, 0, g0, g0, g1};
+        return true;
+      }
+    }
+    return false;
+  };
+  // order: expert, token group, item
+  auto advance = [&](MmaCursor& c) -> bool {
+    if (++c.g < c.g1) return true;
+    if ((c.q + 1) * xtok < rt.off[c.u + 1] - rt.off[c.u]) {
+      ++c.q;
+      c.g = c.g0;
+      return true;
+    }
+    return enter(c, c.u + 1);
+  };
+
+  MmaCursor c;
+  bool ok = enter(c, first_expert(pc, U, lo));
+  uint32_t i = 0;
+
+  if (warp == kMWarps) {  // producer
+    if (lane != 0) return;
+    const uint32_t bytes = (uint32_t)(2 * L.slab + 32 * nblk);
+    for (; ok; ++i, ok = advance(c)) {
+      const uint32_t s = i % S, r = i / S;
+      if (r > 0 && !mbar_wait(empty + 8 * s, (r - 1) & 1)) {
+        if (error_flag) atomicOr(error_flag, 2u);
+        break;
+      }
+      const uint32_t st = ring + s * L.stage;
+      mbar_arrive_expect_tx(full + 8 * s, bytes);
+      const int row0 = rt.expert[c.u] * 2 * I + c.g * kMNeurons;  // < 2^31 (checked on launch)
+      tma_load_3d(st, &tmap, 0, row0, 0, full + 8 * s);
+      tma_load_3d(st + L.slab, &tmap, 0, row0 + I, 0, full + 8 * s);
+      bulk_g2s_nohint(st + 2 * L.slab, gate_up_scale + (size_t)row0 * nblk, (uint32_t)(16 * nblk),
+                      full + 8 * s);
+      bulk_g2s_nohint(st + 2 * L.slab + 16 * nblk, gate_up_scale + (size_t)(row0 + I) * nblk,
+                      (uint32_t)(16 * nblk), full + 8 * s);
+    }
+    // the copies issued last land before the CTA exits
+    for (uint32_t k = i > (uint32_t)S ? i - S : 0u; k < i; ++k)
+      (void)mbar_wait(full + 8 * (k % S), (k / S) & 1);
+    return;
+  }
+
+  // consumers
+  const int g = lane >> 2, tig = lane & 3;
+  const uint32_t xs = base + L.xs, red = base + L.red, scl = base + L.scl + 1024 * warp;
+  int* ktok = reinterpret_cast<int*>(smem + L.ktok);
+  const uint8_t* xg = reinterpret_cast<const uint8_t*>(x) + wait_token;
+  int staged_u = -1, staged_q = -1, par = 0;
+  bool dead = false;
+  for (; ok; ++i, ok = advance(c)) {
+    const uint32_t s = i % S;
+    const uint32_t st = ring + s * L.stage;
+    const int T = rt.off[c.u + 1] - rt.off[c.u];
+    const int* sl = rt.slots + rt.off[c.u] + c.q * xtok;
+    const int nq = min(xtok, T - c.q * xtok);
+    if (c.u != staged_u || c.q != staged_q) {
+      // every consumer is past the previous item's barrier: staged x is free
+      stage_x_f16(xs, L.xstride, ktok, xg, sl, nq, H, K);
+      named_barrier_sync(1, kMThreads);
+      staged_u = c.u;
+      staged_q = c.q;
+    }
+    if (!dead && !mbar_wait(full + 8 * s, (i / S) & 1)) {
+      dead = true;
+      if (lane == 0 && error_flag) atomicOr(error_flag, 2u);
+    }
+    float acc[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[r][k] = 0.0f;
+    if (!dead) {
+      const uint32_t xrow = xs + (uint32_t)((g < nq ? g : 0) * L.xstride + tig * 16);
+      for (int ch = warp; ch < nchunk; ch += kMWarps)
+        mma_chunk(st, H, ch, acc, xrow + (uint32_t)(ch * 512), scl);
+      __syncwarp();  // every lane is done with the stage
+      if (lane == 0) mbar_arrive(empty + 8 * s);
+    }
+    // this lane's two tokens (read before the barrier: the next item may
+    // restage ktok)
+    const int t0 = 2 * tig;
+    const int k0 = (warp < 2 && t0 < nq) ? ktok[t0] : 0;
+    const int k1 = (warp < 2 && t0 + 1 < nq) ? ktok[t0 + 1] : 0;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t a = red + (uint32_t)((((par * kMWarps + warp) * 2 + r) * 32 + lane) * 16);
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(acc[r][0]),
+                   "f"(acc[r][1]), "f"(acc[r][2]), "f"(acc[r][3])
+                   : "memory");
+    }
+    named_barrier_sync(1, kMThreads);
+    if (warp < 2) {  // row tile `warp`: sum the consumer warps' partials
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kMWarps; ++w) {
+        const uint32_t a = red + (uint32_t)((((par * kMWarps + w) * 2 + warp) * 32 + lane) * 16);
+        const float4 v = lds_f32x4(a);
+        sum[0] += v.x;
+        sum[1] += v.y;
+        sum[2] += v.z;
+        sum[3] += v.w;
+      }
+      const int n = c.g * kMNeurons + 8 * warp + g;
+      if (t0 < nq) {
+        const float f = exp2_int(-(k0 >> 1)), f2 = exp2_int(-(k0 - (k0 >> 1)));
+        const float gv = (sum[0] * f) * f2, uv = (sum[2] * f) * f2;
+        h[(size_t)sl[t0] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
+      }
+      if (t0 + 1 < nq) {
+        const float f = exp2_int(-(k1 >> 1)), f2 = exp2_int(-(k1 - (k1 >> 1)));
+        const float gv = (sum[1] * f) * f2, uv = (sum[3] * f) * f2;
+        h[(size_t)sl[t0 + 1] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
+      }
+    }
+    par ^= 1;
+  }
+}
+
+namespace {
+
+// Ring depth for H: the deepest (up to kMMaxStages) that stages 8 tokens,
+// else 0 (unsupported).
+int mma_stages(int H) {
+  for (int S = kMMaxStages; S >= 2; --S)
+    if (mma_layout(H, S).xtok >= kMTokens) return S;
+  return 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 mma_tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// gate_up codes [rows][H] bytes as {128, rows, H/128} with strides {H, 128}:
+// a box {128, 16, H/128} is 16 whole rows, stored as [H/128][16][128] with
+// the 128-byte swizzle.
+bool encode_gate_up_map(CUtensorMap* map, const void* base, uint64_t rows, int H) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = mma_tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {128, rows, (cuuint64_t)(H / 128)};
+  const cuuint64_t strides[2] = {(cuuint64_t)H, 128};
+  const cuuint32_t box[3] = {128, 16, (cuuint32_t)(H / 128)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gate_up_mma_supported(int B, int H, int I, int E, int K) {
+  return B * K <= kStreamMaxSlots && E <= 4096 && H % 512 == 0 && H <= 2048 &&
+         I % kMNeurons == 0 && (long long)E * 2 * I < (1ll << 31) && mma_stages(H) >= 2;
+}
+
+// p.cpl: ring stages (0: the deepest that fits).
+cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                               bool pdl) {
+  if (!gate_up_mma_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+  int S = mma_stages(a.H);
+  if (p.cpl >= 2 && p.cpl < S) S = p.cpl;
+  const int smem = mma_layout(a.H, S).total;
+  static int configured = 0;
+  if (configured < smem) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(moe_gate_up_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  CUtensorMap map;
+  if (!encode_gate_up_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(kMThreads + 32);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_gate_up_mma, map, reinterpret_cast<const __nv_bfloat16*>(a.x),
+                            a.topk_ids, a.gate_up_scale, reinterpret_cast<__nv_bfloat16*>(a.h),
+                            a.error_flag, a.B, a.H, a.I, a.E, a.K, S);
+}
+
+}  // namespace wd

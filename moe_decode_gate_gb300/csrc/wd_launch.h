@@ -41,6 +41,7 @@ enum GateUpVariant {
   kGateUpPersist = 4,   // moe_gate_up_persist: one wave of CTAs over shared expert rows, x staged
   kGateUpRing = 5,      // moe_gate_up_ring: as persist, rows through a per-warp bulk-copy ring
   kGateUpTma = 6,       // moe_gate_up_tma: as persist, rows by 2-D TMA into a CTA-wide ring
+  kGateUpMma = 7,       // moe_gate_up_mma: as persist, products by warp-level tensor-core MMAs
 };
 
 // Compile-time shape of one kernel instance.
@@ -67,6 +68,7 @@ DownPlan plan_down(int B, int H, int I, int K, int E);
 // The plans above, downgraded to a non-streamed kernel when the bulk copies'
 // 16-byte alignment does not hold for the given pointers.
 GateUpPlan plan_gate_up_for(const GateUpArgs& a);
+int pdl_mask_for(const GateUpPlan& g);
 DownPlan plan_down_for(const DownArgs& a);
 
 cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream, bool pdl);
@@ -87,6 +89,9 @@ bool gate_up_ring_supported(int B, int H, int I, int E, int K, int stages);
 cudaError_t launch_gate_up_tma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                bool pdl);
 bool gate_up_tma_supported(int B, int H, int I, int E, int K);
+cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                               bool pdl);
+bool gate_up_mma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_stream_supported(int B, int H, int I, int E, int K);

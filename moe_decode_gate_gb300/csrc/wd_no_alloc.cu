@@ -82,11 +82,13 @@ extern "C" wd_status wd_moe_decode_no_alloc(const void* x, const int32_t* topk_i
   // element the second kernel reads (zeros for out-of-range ids).  No error
   // flag is kept: out-of-range ids contribute nothing and are not reported.
   const wd::GateUpArgs ga{x, topk_ids, gate_up, gate_up_scale, h, nullptr, B, H, I, E, K};
-  cudaError_t e = wd::launch_gate_up(ga, wd::plan_gate_up_for(ga), s, true);
+  const wd::GateUpPlan gp = wd::plan_gate_up_for(ga);
+  const int pdl = wd::pdl_mask_for(gp);
+  cudaError_t e = wd::launch_gate_up(ga, gp, s, (pdl & 1) != 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return WD_ERR_CUDA;
   const wd::DownArgs da{h, topk_ids, topk_w, down, down_scale, out, nullptr, B, H, I, E, K};
-  e = wd::launch_down(da, wd::plan_down_for(da), s, true);
+  e = wd::launch_down(da, wd::plan_down_for(da), s, (pdl & 2) != 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? WD_OK : WD_ERR_CUDA;
 }

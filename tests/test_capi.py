@@ -137,20 +137,22 @@ def test_built_in_plan_by_batch():
     wd.wd_moe_set_plan(None)
     q = dict(H=2048, I=768, E=128, K=8)
     assert wd.wd_moe_describe_plan(1, **q) == \
-        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6>"
+        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6> pdl=3"
     assert wd.wd_moe_describe_plan(2, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3>"
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3> pdl=3"
     assert wd.wd_moe_describe_plan(4, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1>"
-    for B in (8, 16, 32):
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1> pdl=3"
+    for B in (8, 16, 32):  # tokens share experts: tensor-core gate/up, down not overlapped
         assert wd.wd_moe_describe_plan(B, **q) == \
-            "gate_up=moe_gate_up_persist<2,1> down=moe_down_3d_batched<4,1>"
+            "gate_up=moe_gate_up_mma<8,0> down=moe_down_3d_batched<4,1> pdl=1"
+    # H above the tensor-core kernel's limit: the CUDA-core persistent kernel
+    assert wd.wd_moe_describe_plan(32, 4096, 768, 128, 8).startswith("gate_up=moe_gate_up_persist<2,1>")
     # B*K above the persistent kernel's routing tables: the shared-row kernel
     assert wd.wd_moe_describe_plan(64, **q).startswith("gate_up=moe_gate_up_rowshare<2,2>")
     wd.wd_moe_set_plan("gu=batched:1:2,dn=shared:4")
     try:
         assert wd.wd_moe_describe_plan(32, **q) == \
-            "gate_up=moe_gate_up_3d_batched<1,2> down=moe_down_shared<4,0>"
+            "gate_up=moe_gate_up_3d_batched<1,2> down=moe_down_shared<4,0> pdl=3"
     finally:
         wd.wd_moe_set_plan(None)
     lib = wd.lib()
@@ -168,6 +170,9 @@ def test_plan_override_parser():
     assert lib.wd_moe_set_plan(b"gu=persist:1:1,dn=shared:2") == OK
     assert lib.wd_moe_set_plan(b"gu=tma,dn=4:1") == OK
     assert lib.wd_moe_set_plan(b"gu=ring:2") == OK
+    assert lib.wd_moe_set_plan(b"gu=mma,pdl=3") == OK
+    assert lib.wd_moe_set_plan(b"gu=mma:2,pdl=0") == OK
+    assert lib.wd_moe_set_plan(b"pdl=4") == INVALID
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID
     assert lib.wd_moe_set_plan(None) == OK

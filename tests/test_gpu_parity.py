@@ -13,7 +13,7 @@ import oracle
 import synth
 import moe_decode_gate_gb300 as wd
 
-from parity import compare, from_dev_bf16, to_dev, to_dev_bf16
+from parity import bf16_bits_to_f64, compare, from_dev_bf16, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -246,6 +246,7 @@ PLANS = [
     "gu=ring:3,dn=2:3",
     "gu=tma,dn=4:1",
     "gu=batched:2:1,dn=shared:2",
+    "gu=mma,dn=4:1",
 ]
 
 PLAN_SHAPES = [
@@ -286,7 +287,8 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
                                   "gu=persist:2:2,dn=persist:4:1",
                                   "gu=persist:2:2,dn=shared:4",
                                   "gu=ring:2,dn=4:1",
-                                  "gu=tma,dn=4:1"])
+                                  "gu=tma,dn=4:1",
+                                  "gu=mma,dn=4:1"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
@@ -317,3 +319,90 @@ def test_fp16_product_path_keeps_tokens_fp16_cannot_hold_exact(cuda_device, plan
     xf[5, 1000] = 2.0 ** -18
     xs = xf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"{plan} fp16 boundary tokens")
+
+
+# moe_gate_up_mma: B*K <= 256, H % 512 == 0, H <= 2048, I % 16 == 0.  Shapes:
+# the full-size layer at B = 8..32 with every routing pattern of the benchmark
+# (fixed: 32 tokens per expert, four groups of 8 staged tokens; disjoint: 2 per
+# expert), B*K = 256 (the table limit), two 256-column chunks per row (six
+# consumer warps idle), six chunks (H = 1536), ~13 tokens per expert (two
+# groups, the second partly empty), K == E, and a single token.
+MMA_SHAPES = [
+    (8, 2048, 768, 128, 8, "uniform"),
+    (16, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "zipf"),
+    (32, 2048, 768, 128, 8, "fixed"),
+    (32, 2048, 768, 128, 8, "disjoint"),
+    (64, 2048, 768, 128, 4, "uniform"),
+    (5, 512, 64, 4, 2, "uniform"),
+    (10, 1536, 32, 4, 2, "uniform"),
+    (40, 1024, 128, 6, 2, "uniform"),
+    (3, 1024, 256, 3, 3, "uniform"),
+    (1, 2048, 768, 128, 8, "uniform"),
+]
+
+
+@pytest.mark.parametrize("B,H,I,E,K,route", MMA_SHAPES)
+def test_gate_up_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
+    wd.wd_moe_set_plan("gu=mma,dn=4:1")
+    assert "gate_up=moe_gate_up_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
+    xs, ids, w, gu, gus, dn, dns = _random_case(900 + B + H + I + E, B, H, I, E, K, route=route)
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"gu=mma B={B} H={H} I={I} {route}")
+
+
+def test_gate_up_mma_activation_range(cuda_device, plan_reset):
+    """Tokens are re-encoded in FP16 with a per-token power-of-two scale: an
+    ordinary token; one of magnitude 1e-15 (scaled up); one of 1e+15 (scaled
+    down); all zeros; BF16 subnormals only; and a wide dynamic range (1e-12
+    next to 1e+3), whose smallest values sit below the FP16 grid."""
+    wd.wd_moe_set_plan("gu=mma,dn=4:1")
+    xs, ids, w, gu, gus, dn, dns = _random_case(31, 6, 1024, 256, 8, 3)
+    xf = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).float()
+    xf[1] *= 1e-15
+    xf[2] *= 1e15
+    xf[3, :] = 0.0
+    xf[4] = torch.sign(xf[4]) * 2.0 ** -130
+    xf[5, ::2] *= 1e-12
+    xf[5, 1] = 1e3
+    xs = xf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    I, E = 256, 8
+    want_h = oracle.gate_up(xs, ids, gu, gus, I, E)
+    h = torch.empty((6, 3, I), dtype=torch.bfloat16, device=cuda_device)
+    wd.wd_moe_gate_up(to_dev_bf16(xs, cuda_device), to_dev(ids, cuda_device),
+                      to_dev(gu, cuda_device), to_dev(gus, cuda_device), h)
+    torch.cuda.synchronize()
+    got_h = from_dev_bf16(h)
+    for t in range(6):  # per token: each has its own output scale
+        compare(got_h[t].reshape(-1, I), want_h[t].reshape(-1, I), f"gu=mma token {t}")
+
+
+def test_gate_up_mma_special_scale_codes(cuda_device, plan_reset):
+    """E8M0 code 0 (2^-127) on whole rows and code 255 (NaN) on one block: the
+    NaN reaches exactly the outputs of that row, the rest matches the oracle."""
+    wd.wd_moe_set_plan("gu=mma,dn=4:1")
+    B, H, I, E, K = 4, 512, 128, 4, 2
+    xs, ids, w, gu, gus, dn, dns = _random_case(33, B, H, I, E, K)
+    ids = np.array([[0, 1], [1, 2], [0, 3], [2, 1]], dtype=np.int32)
+    gus = gus.copy()
+    gu = gu.copy()
+    gus[1, 5, :] = 0        # gate row 5 of expert 1: every block at 2^-127
+    gu[1, 5, :] = 0x70      # E4M3 128: products of ~2^-120 |x|
+    gus[2, I + 7, 3] = 255  # up row 7 of expert 2: one NaN block
+    want_h = oracle.gate_up(xs, ids, gu, gus, I, E)
+    h = torch.empty((B, K, I), dtype=torch.bfloat16, device=cuda_device)
+    wd.wd_moe_gate_up(to_dev_bf16(xs, cuda_device), to_dev(ids, cuda_device),
+                      to_dev(gu, cuda_device), to_dev(gus, cuda_device), h)
+    torch.cuda.synchronize()
+    got = bf16_bits_to_f64(from_dev_bf16(h)).reshape(B, K, I)
+    want = bf16_bits_to_f64(want_h).reshape(B, K, I)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.isnan(want).sum() == 2  # tokens 1 and 3 route expert 2 once each
+    tiny = [(0, 1, 5), (1, 0, 5), (3, 1, 5)]  # (token, slot, neuron) through gate row 5 of expert 1
+    for t, k, n in tiny:
+        assert 0.0 < abs(want[t, k, n]) < 2.0 ** -100
+        assert abs(got[t, k, n] - want[t, k, n]) <= 2.0 ** -7 * abs(want[t, k, n])
+    got[np.isnan(got)] = 0.0
+    want[np.isnan(want)] = 0.0
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * np.abs(want).max() + 2e-3
