@@ -150,6 +150,8 @@ WD_API int wd_moe_launches_per_call(void);
  *   "dn=<output dims per warp>:<blocks per lane per pass>"
  *   "dn=persist:<output dims per warp>:<blocks per lane per pass>"
  *   "dn=stream:<stages>" | "dn=shared:<output dims per CTA>"
+ *   "dn=mma[:<ring stages, 2..4>]"  (tensor-core products; B <= 64,
+ *                                    B*K <= 256, H % 16 == 0, I % 128 == 0)
  *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel
  *                    where the persistent one does not apply>"
  *   "pdl=<0..3>" (programmatic dependent launch: bit 0 lets the gate/up

@@ -24,7 +24,8 @@ namespace wd {
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
 //   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma" |
 //   "gu=mma[:<stages>]",
-//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>",
+//   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>" |
+//   "dn=mma[:<stages>]",
 //   "rowshare_min_b=<B>", "pdl=<mask>" (bit 0: the gate/up launch may overlap the
 //   kernel before it, bit 1: the down launch may overlap gate/up), comma-separated;
 //   "" or NULL restores the defaults.
@@ -82,6 +83,12 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpRowShare;
         p.gu_npw = a;
         p.gu_cpl = b;
+      } else if (sscanf(tok, "dn=mma:%d", &a) == 1) {
+        p.dn_variant = kDownMma;
+        p.dn_qpl = a;
+      } else if (strcmp(tok, "dn=mma") == 0) {
+        p.dn_variant = kDownMma;
+        p.dn_qpl = 0;
       } else if (sscanf(tok, "dn=stream:%d", &a) == 1) {
         p.dn_variant = kDownStream;
         p.dn_qpl = a;
@@ -157,6 +164,8 @@ DownPlan plan_down(int B, int H, int I, int K, int E) {
   if (o.dn_variant == kDownPersist) return DownPlan{o.dn_rpw, o.dn_qpl, kDownPersist};
   if (o.dn_variant == kDownShared && down_shared_supported(B, H, I, E, K, o.dn_rpw))
     return DownPlan{o.dn_rpw, 0, kDownShared};
+  if (o.dn_variant == kDownMma && down_mma_supported(B, H, I, E, K))
+    return DownPlan{16, o.dn_qpl, kDownMma};
   if (B >= 4) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
   const int nq = K * (I / 32);
   const int per_lane = (nq + 31) / 32;
@@ -190,7 +199,9 @@ GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
 
 DownPlan plan_down_for(const DownArgs& a) {
   DownPlan p = plan_down(a.B, a.H, a.I, a.K, a.E);
-  if (p.variant == kDownStream && !(aligned16(a.down) && aligned16(a.down_scale))) {
+  if ((p.variant == kDownStream && !(aligned16(a.down) && aligned16(a.down_scale))) ||
+      (p.variant == kDownMma &&
+       !(aligned16(a.down) && aligned16(a.down_scale) && aligned16(a.h)))) {
     const int per_lane = (a.K * (a.I / 32) + 31) / 32;
     p = DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
   }
@@ -346,9 +357,10 @@ wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, siz
                                          "moe_gate_up_persist", "moe_gate_up_ring",
                                          "moe_gate_up_tma", "moe_gate_up_mma"};
   static const char* const dn_names[] = {"moe_down_3d_batched", "moe_down_stream",
-                                         "moe_down_3d_batched_persist", "moe_down_shared"};
+                                         "moe_down_3d_batched_persist", "moe_down_shared",
+                                         "moe_down_mma"};
   const char* gn = (g.variant >= 0 && g.variant <= 7) ? gu_names[g.variant] : "?";
-  const char* dn = (d.variant >= 0 && d.variant <= 3) ? dn_names[d.variant] : "?";
+  const char* dn = (d.variant >= 0 && d.variant <= 4) ? dn_names[d.variant] : "?";
   snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d> pdl=%d", gn, g.npw, g.cpl, dn, d.rpw,
            d.qpl, wd::pdl_mask_for(g));
   return WD_OK;

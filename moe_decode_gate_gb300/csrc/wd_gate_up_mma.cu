@@ -56,10 +56,8 @@
 // runs out raises bit 1 of the error flag and computes nothing more but keeps
 // following the consumers' barriers; the producer stops issuing when its wait
 // runs out, and before exiting waits (bounded) for the copies it issued last.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "wd_launch.h"
+#include "wd_mma.cuh"
 #include "wd_persist.cuh"
 
 namespace wd {
@@ -114,91 +112,6 @@ __host__ __device__ inline MmaLayout mma_layout(int H, int S) {
   L.total = L.scl + kMScaleBytes;
   return L;
 }
-
-// Byte offset of (row, col) in a 128-byte-swizzled slab [H/128][16][128]:
-// 16-byte chunk q of a 128-byte line is stored at q ^ (row % 8).
-__device__ __forceinline__ uint32_t slab_offset(int row, int col) {
-  return (uint32_t)((col >> 7) * 2048 + row * 128 + ((((col & 127) >> 4) ^ (row & 7)) << 4) +
-                    (col & 15));
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-// Bulk copy global -> shared without an L2 cache hint.
-__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
-                                                uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Two E4M3 codes (low 16 bits of w) -> f16x2, element 0 in the low half (exact).
-__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t}"
-      : "=r"(r)
-      : "r"(w));
-  return r;
-}
-__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}"
-      : "=r"(r)
-      : "r"(w));
-  return r;
-}
-
-// d = A(16x16, f16) * B(16x8, f16), FP32 accumulate from zero.
-__device__ __forceinline__ void mma_f16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                             uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
-}
-// d += A * B.
-__device__ __forceinline__ void mma_f16_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                            uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-
-// 16 bytes of activations written by an earlier kernel: coherent load; `p`
-// must depend on grid_dependency_wait()'s token.
-__device__ __forceinline__ uint4 ld_act_16B(const void* p) {
-  uint4 r;
-  asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t w) {
-  return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
-}
-
-// Exponent k such that 2^k times the largest magnitude (BF16 bits `mx`,
-// sign cleared) lies in [2^14, 2^15); 0 for an all-zero row or a row holding
-// Inf or NaN (whose results are not finite anyway).
-__device__ __forceinline__ int fp16_row_exponent(uint32_t mx) {
-  if (mx == 0u || mx >= 0x7F80u) return 0;
-  const int ef = (int)(mx >> 7);
-  const int e = ef ? ef - 127 : (31 - __clz((int)mx)) - 133;  // floor(log2(largest magnitude))
-  return 14 - e;
-}
-
-// 2^k for k in [-126, 127].
-__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
 
 // Stage the x rows of tokens slots[0..nq) (token b = slot / K) in shared
 // memory as FP16 scaled by 2^k_t, row t at xs + t * stride, and k_t in
@@ -507,34 +420,6 @@ int mma_stages(int H) {
   return 0;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 mma_tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// gate_up codes [rows][H] bytes as {128, rows, H/128} with strides {H, 128}:
-// a box {128, 16, H/128} is 16 whole rows, stored as [H/128][16][128] with
-// the 128-byte swizzle.
-bool encode_gate_up_map(CUtensorMap* map, const void* base, uint64_t rows, int H) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = mma_tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {128, rows, (cuuint64_t)(H / 128)};
-  const cuuint64_t strides[2] = {(cuuint64_t)H, 128};
-  const cuuint32_t box[3] = {128, 16, (cuuint32_t)(H / 128)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool gate_up_mma_supported(int B, int H, int I, int E, int K) {
@@ -557,7 +442,7 @@ cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStr
     configured = smem;
   }
   CUtensorMap map;
-  if (!encode_gate_up_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H))
+  if (!encode_row_slab_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

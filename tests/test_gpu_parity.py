@@ -247,6 +247,8 @@ PLANS = [
     "gu=tma,dn=4:1",
     "gu=batched:2:1,dn=shared:2",
     "gu=mma,dn=4:1",
+    "gu=mma,dn=mma",
+    "gu=persist:2:1,dn=mma:2",
 ]
 
 PLAN_SHAPES = [
@@ -288,7 +290,8 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
                                   "gu=persist:2:2,dn=shared:4",
                                   "gu=ring:2,dn=4:1",
                                   "gu=tma,dn=4:1",
-                                  "gu=mma,dn=4:1"])
+                                  "gu=mma,dn=4:1",
+                                  "gu=batched:2:1,dn=mma"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
@@ -402,6 +405,96 @@ def test_gate_up_mma_special_scale_codes(cuda_device, plan_reset):
     for t, k, n in tiny:
         assert 0.0 < abs(want[t, k, n]) < 2.0 ** -100
         assert abs(got[t, k, n] - want[t, k, n]) <= 2.0 ** -7 * abs(want[t, k, n])
+    got[np.isnan(got)] = 0.0
+    want[np.isnan(want)] = 0.0
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * np.abs(want).max() + 2e-3
+
+
+# moe_down_mma: B <= 64, B*K <= 256, H % 16 == 0, I % 128 == 0.  Shapes: the
+# full-size layer at B = 8..64 with every routing pattern (fixed: 32 pairs per
+# expert, four groups of 8; disjoint: 2 per expert), two CTAs (H = 32), I = 128
+# (one block per consumer warp and none for the others), ~13 pairs per expert
+# (a second, partly empty group), duplicate-prone K == E, and a single token.
+DN_MMA_SHAPES = [
+    (8, 2048, 768, 128, 8, "uniform"),
+    (16, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "zipf"),
+    (32, 2048, 768, 128, 8, "fixed"),
+    (32, 2048, 768, 128, 8, "disjoint"),
+    (64, 2048, 768, 128, 4, "uniform"),
+    (2, 32, 128, 2, 2, "uniform"),
+    (40, 1024, 128, 6, 2, "uniform"),
+    (3, 512, 384, 3, 3, "uniform"),
+    (1, 2048, 768, 128, 8, "uniform"),
+]
+
+
+@pytest.mark.parametrize("B,H,I,E,K,route", DN_MMA_SHAPES)
+def test_down_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
+    wd.wd_moe_set_plan("dn=mma")
+    assert "down=moe_down_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
+    xs, ids, w, gu, gus, dn, dns = _random_case(1100 + B + H + I + E, B, H, I, E, K, route=route)
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"dn=mma B={B} H={H} I={I} {route}")
+
+
+def _down_alone(dev, h_bits, ids, w, dn, dns, H, E):
+    B, K, I = h_bits.shape
+    want = oracle.down(h_bits, ids, w, dn, dns, H, E)
+    out = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    wd.wd_moe_down(to_dev_bf16(h_bits, dev), to_dev(ids, dev), to_dev(w, dev), to_dev(dn, dev),
+                   to_dev(dns, dev), out, error_flag=flag)
+    torch.cuda.synchronize()
+    return from_dev_bf16(out), want, int(flag.item())
+
+
+def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset):
+    """h rows are re-encoded per (token, slot) as FP16 times a power of two:
+    ordinary rows, rows of magnitude 1e-20 and 1e+20, an all-zero row, BF16
+    subnormals only, a row spanning 1e-12 .. 1e+3; a token routed twice to one
+    expert and a zero routing weight."""
+    wd.wd_moe_set_plan("dn=mma")
+    B, H, I, E, K = 6, 256, 256, 4, 3
+    xs, ids, w, gu, gus, dn, dns = _random_case(41, B, H, I, E, K)
+    ids, w = ids.copy(), w.copy()
+    ids[0, 2] = ids[0, 1]
+    w[3, 0] = 0.0
+    h = oracle.gate_up(xs, ids, gu, gus, I, E)
+    hf = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).float()
+    hf[1] *= 1e-20
+    hf[2] *= 1e20
+    hf[3, 1, :] = 0.0
+    hf[4, 0] = torch.sign(hf[4, 0]) * 2.0 ** -130
+    hf[5, 2, ::2] *= 1e-12
+    hf[5, 2, 1] = 1e3
+    hb = hf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got, want, flag = _down_alone(cuda_device, hb, ids, w, dn, dns, H, E)
+    assert flag == 0
+    for t in range(B):  # per token: the rows differ by up to 40 orders of magnitude
+        compare(got[t:t + 1], want[t:t + 1], f"dn=mma token {t}")
+
+
+def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset):
+    """E8M0 codes far from 1 (2^-40 .. 2^+19), 0 (2^-127) on a whole row and 255
+    (NaN) on one block; an out-of-range id contributes nothing and is flagged."""
+    wd.wd_moe_set_plan("dn=mma")
+    B, H, I, E, K = 4, 128, 256, 4, 2
+    xs, ids, w, gu, gus, dn, dns = _random_case(43, B, H, I, E, K)
+    ids = np.array([[0, 1], [1, 2], [0, 9], [2, 3]], dtype=np.int32)
+    rng = np.random.default_rng(5)
+    dns = (127 + rng.integers(-40, 20, dns.shape)).astype(np.uint8)
+    dn = dn.copy()
+    dn[..., ::32] = rng.integers(1, 8, dn[..., ::32].shape)  # subnormal E4M3 codes
+    dns[3, 7, :] = 0       # expert 3, output dim 7: every block at 2^-127
+    dns[1, 20, 2] = 255    # expert 1, output dim 20: one NaN block
+    h = oracle.gate_up(xs, ids, gu, gus, I, E)
+    got_b, want_b, flag = _down_alone(cuda_device, h, ids, w, dn, dns, H, E)
+    assert flag == 1
+    got, want = bf16_bits_to_f64(got_b), bf16_bits_to_f64(want_b)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.isnan(want[:, 20]).sum() == 2  # tokens 0 and 1 route expert 1
     got[np.isnan(got)] = 0.0
     want[np.isnan(want)] = 0.0
     err = np.abs(got - want).max()
