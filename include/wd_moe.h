@@ -144,7 +144,8 @@ WD_API int wd_moe_launches_per_call(void);
  *   "gu=rowshare:<neurons per warp>:<words per step>"   (tokens share rows)
  *   "gu=persist:<neurons per warp>:<1 + L2 prefetch distance>"
  *   "gu=ring:<bulk-copy ring stages per warp>" | "gu=tma" |
- *   "gu=mma[:<ring stages, 2..4>]"  (tensor-core products; B*K <= 256,
+ *   "gu=mma[:<ring stages, 2..4>[:<consumer warps, 8 or 16>]]"
+ *                                   (tensor-core products; B*K <= 256,
  *                                    H % 512 == 0, H <= 2048, I % 16 == 0)
  *   "gu=stream:<variant>:<stages>" | "gu=mixed:<variant>:<stages>"
  *   "dn=<output dims per warp>:<blocks per lane per pass>"

@@ -23,7 +23,7 @@ namespace wd {
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=stream:<npw>:<stages>" |
 //   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma" |
-//   "gu=mma[:<stages>]",
+//   "gu=mma[:<stages>[:<consumer warps, 8 or 16>]]",
 //   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>" |
 //   "dn=mma[:<stages>]",
 //   "rowshare_min_b=<B>", "pdl=<mask>" (bit 0: the gate/up launch may overlap the
@@ -59,6 +59,10 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpStream;
         p.gu_npw = a;
         p.gu_cpl = b;
+      } else if (sscanf(tok, "gu=mma:%d:%d", &a, &b) == 2) {
+        p.gu_variant = kGateUpMma;
+        p.gu_npw = b;
+        p.gu_cpl = a;
       } else if (sscanf(tok, "gu=mma:%d", &a) == 1) {
         p.gu_variant = kGateUpMma;
         p.gu_npw = 8;
@@ -142,7 +146,7 @@ GateUpPlan plan_gate_up(int B, int H, int I, int K, int E) {
   if (o.gu_variant == kGateUpTma && gate_up_tma_supported(B, H, I, E, K))
     return {kGateUpTma, 2, 3};
   if (o.gu_variant == kGateUpMma && gate_up_mma_supported(B, H, I, E, K))
-    return {kGateUpMma, 8, o.gu_cpl};
+    return {kGateUpMma, o.gu_npw == 16 ? 16 : 8, o.gu_cpl};
   if (o.gu_variant == kGateUpBatched) return {kGateUpBatched, o.gu_npw, o.gu_cpl};
   // built-in, from GB300 measurements on the 48-layer Qwen-3-style stack
   // (H=2048, I=768, E=128, K=8): one warp per (token, slot, neuron group) while

@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_down_mma(
 
   // consumers
   const int g = lane >> 2, tig = lane & 3;
+  const int pg = slab_row(g);  // the down row (output dim) of tile rows g and g + 8
   const uint32_t table = base + L.tables + warp * kDRows * B * 4;
   bool dead = false;
   if (U > 0) {
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_down_mma(
       const uint32_t brow = st + L.hrows + (g < nq ? g : 0) * L.hpitch + tig * 16;
       for (int j = warp; j < nbi; j += kDWarps) {
         const int col = j * 32 + tig * 8;
-        const uint2 w0 = lds_u32x2(st + slab_offset(g, col));
-        const uint2 w1 = lds_u32x2(st + slab_offset(g + 8, col));
+        const uint2 w0 = lds_u32x2(st + slab_offset(pg, col));
+        const uint2 w1 = lds_u32x2(st + slab_offset(pg + 8, col));
         const uint4 b = lds_u32x4(brow + j * 64);
         // columns 8 tig + 0..3 (first k16 step) and 8 tig + 4..7 (second)
         float cc[4];
@@ -287,8 +288,8 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_down_mma(
                      e4m3x2_hi_to_f16x2(w0.x), e4m3x2_hi_to_f16x2(w1.x), b.x, b.y);
         mma_f16_acc(cc, e4m3x2_lo_to_f16x2(w0.y), e4m3x2_lo_to_f16x2(w1.y),
                     e4m3x2_hi_to_f16x2(w0.y), e4m3x2_hi_to_f16x2(w1.y), b.z, b.w);
-        const float s0 = lds_f32(st + L.scales + (g * nbi + j) * 4);
-        const float s1 = lds_f32(st + L.scales + ((g + 8) * nbi + j) * 4);
+        const float s0 = lds_f32(st + L.scales + (pg * nbi + j) * 4);
+        const float s1 = lds_f32(st + L.scales + ((pg + 8) * nbi + j) * 4);
         acc[0] = fmaf(cc[0], s0, acc[0]);
         acc[1] = fmaf(cc[1], s0, acc[1]);
         acc[2] = fmaf(cc[2], s1, acc[2]);
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(kDThreads, 1) moe_down_mma(
         const float wv = __uint_as_float(info[q].x);
         const int k = (int)info[q].y, tok = (int)info[q].z;
         const float f1 = exp2_int(-(k >> 1)), f2 = exp2_int(-(k - (k >> 1)));
-        red_add_shared(table + (uint32_t)((g * B + tok) * 4), ((acc[q] * wv) * f1) * f2);
-        red_add_shared(table + (uint32_t)(((g + 8) * B + tok) * 4), ((acc[2 + q] * wv) * f1) * f2);
+        red_add_shared(table + (uint32_t)((pg * B + tok) * 4), ((acc[q] * wv) * f1) * f2);
+        red_add_shared(table + (uint32_t)(((pg + 8) * B + tok) * 4), ((acc[2 + q] * wv) * f1) * f2);
       }
     }
   }

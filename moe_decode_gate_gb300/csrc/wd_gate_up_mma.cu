@@ -64,13 +64,14 @@ namespace wd {
 
 namespace {
 
-constexpr int kMWarps = 8;                 // consumer warps
-constexpr int kMThreads = 32 * kMWarps;
+constexpr int kMMaxWarps = 16;            // consumer warps (8 or 16; 2048 / 16 = 128 columns each)
 constexpr int kMTokens = 8;                // tokens staged at once: one MMA column tile
 constexpr int kMNeurons = 16;              // neurons per item: two 16-row MMA tiles
 constexpr int kMItemBase = 8;              // item cost = groups * kMItemBase + 1
-constexpr int kMRedBytes = 2 * kMWarps * 2 * 32 * 16;  // [2 parities][warps][2 tiles][32] float4
-constexpr int kMScaleBytes = kMWarps * 1024;          // per-warp FP32 tables [32 rows][8 blocks]
+// partial sums [2 parities][warps][2 tiles][32 lanes] float4, and per-warp FP32
+// scale tables [32 rows][blocks per chunk]: 32 KiB + 8 KiB for either warp count
+constexpr int kMRedBytes = 2 * kMMaxWarps * 2 * 32 * 16;
+constexpr int kMScaleBytes = 8 * 1024;
 constexpr int kMSmemCap = 227 * 1024;
 constexpr int kMMaxStages = 4;
 
@@ -117,10 +118,10 @@ __host__ __device__ inline MmaLayout mma_layout(int H, int S) {
 // memory as FP16 scaled by 2^k_t, row t at xs + t * stride, and k_t in
 // ktok[t].  Warp w converts tokens w, w + 8, ...; no barrier.
 __device__ __forceinline__ void stage_x_f16(uint32_t xs, int stride, int* ktok, const uint8_t* xg,
-                                            const int* slots, int nq, int H, int K) {
+                                            const int* slots, int nq, int H, int K, int nwarps) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nch = H >> 3;  // 16-byte chunks of 8 BF16 values
-  for (int t = warp; t < nq; t += kMWarps) {
+  for (int t = warp; t < nq; t += nwarps) {
     const uint8_t* row = xg + (size_t)(slots[t] / K) * H * 2;
     uint32_t mx = 0u;
     for (int i = lane; i < nch; i += 32) {
@@ -175,41 +176,48 @@ __device__ __forceinline__ void mma_cost_prefix(const RoutingTables& rt, int nb,
   __syncthreads();
 }
 
-// acc[r] += the contribution of 256-column chunk c of the item held in ring
-// stage `st`, for row tile r = 0, 1.  `xrow` is the shared-memory address of
-// this lane's staged activation row (token g of the group) at column 0 of the
-// chunk plus 16 * tig.  `scl` is this warp's 1 KiB table, into which the
-// chunk's 256 scale codes (32 rows x 8 blocks) are decoded first.
+// acc[r] += the contribution of chunk c (CB blocks of 32 columns) of the item
+// held in ring stage `st`, for row tile r = 0, 1.  `xrow` is the shared-memory
+// address of this lane's staged activation row (token g of the group) at
+// column 0 of the chunk plus 16 * tig.  `scl` is this warp's table, into which
+// the chunk's 32 x CB scale codes are decoded first (FP32 [32 rows][CB]).
+template <int CB>
 __device__ __forceinline__ void mma_chunk(uint32_t st, int H, int c, float (&acc)[2][4],
                                           uint32_t xrow, uint32_t scl) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  static_assert(CB == 4 || CB == 8, "4 or 8 blocks per chunk");
+  const int lane = threadIdx.x & 31, g = slab_row(lane >> 2), tig = lane & 3;
   const int nblk = H >> 5;
   const uint32_t gate = st, up = st + 16 * H, sc = st + 32 * H;
   // lane l decodes table row l (gate rows 0..15, then up rows 0..15), blocks
-  // 8c .. 8c + 7
-  const uint2 codes = lds_u32x2(sc + lane * nblk + c * 8);
+  // CB c .. CB c + CB - 1
+  uint32_t code[CB / 4];
+  if (CB == 8) {
+    const uint2 v = lds_u32x2(sc + lane * nblk + c * CB);
+    code[0] = v.x;
+    code[CB / 4 - 1] = v.y;
+  } else {
+    code[0] = lds_u32(sc + lane * nblk + c * CB);
+  }
   __syncwarp();  // the previous chunk's scale reads are done
-  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 32 * lane),
-               "f"(e8m0_to_f32(codes.x & 0xFFu)), "f"(e8m0_to_f32((codes.x >> 8) & 0xFFu)),
-               "f"(e8m0_to_f32((codes.x >> 16) & 0xFFu)), "f"(e8m0_to_f32(codes.x >> 24))
-               : "memory");
-  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 32 * lane + 16),
-               "f"(e8m0_to_f32(codes.y & 0xFFu)), "f"(e8m0_to_f32((codes.y >> 8) & 0xFFu)),
-               "f"(e8m0_to_f32((codes.y >> 16) & 0xFFu)), "f"(e8m0_to_f32(codes.y >> 24))
-               : "memory");
+#pragma unroll
+  for (int q = 0; q < CB / 4; ++q)
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 4 * CB * lane + 16 * q),
+                 "f"(e8m0_to_f32(code[q] & 0xFFu)), "f"(e8m0_to_f32((code[q] >> 8) & 0xFFu)),
+                 "f"(e8m0_to_f32((code[q] >> 16) & 0xFFu)), "f"(e8m0_to_f32(code[q] >> 24))
+                 : "memory");
   __syncwarp();
   float4 sg4[2], su4[2];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < CB; ++j) {
     if ((j & 3) == 0) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        sg4[r] = lds_f32x4(scl + 32 * (8 * r + g) + 4 * j);
-        su4[r] = lds_f32x4(scl + 32 * (16 + 8 * r + g) + 4 * j);
+        sg4[r] = lds_f32x4(scl + 4 * CB * (8 * r + g) + 4 * j);
+        su4[r] = lds_f32x4(scl + 4 * CB * (16 + 8 * r + g) + 4 * j);
       }
     }
     const uint4 b = lds_u32x4(xrow + 64 * j);
-    const int col = c * 256 + j * 32 + tig * 8;
+    const int col = c * 32 * CB + j * 32 + tig * 8;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const float sg = (j & 3) == 0 ? sg4[r].x : (j & 3) == 1 ? sg4[r].y : (j & 3) == 2 ? sg4[r].z : sg4[r].w;
@@ -240,10 +248,13 @@ struct MmaCursor {
 
 }  // namespace
 
-// Threads: kMWarps consumer warps, then one producer warp.  `S`: ring stages.
-// `tmap`: the gate/up codes as a 3-D byte tensor {128, E * 2I, H / 128} with
-// strides {H, 128}, boxes {128, 16, H / 128}, 128-byte swizzle.
-__global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
+// Threads: NW consumer warps (each owns chunks of 2048 / NW columns of an
+// item: 8 warps x 256 or 16 warps x 128 at H = 2048), then one producer warp.
+// `S`: ring stages.  `tmap`: the gate/up codes as a 3-D byte tensor
+// {128, E * 2I, H / 128} with strides {H, 128}, boxes {128, 16, H / 128},
+// 128-byte swizzle.
+template <int NW>
+__global__ void __launch_bounds__(32 * NW + 32, 1) moe_gate_up_mma(
     const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16* __restrict__ x,
     const int32_t* __restrict__ topk_ids, const uint8_t* __restrict__ gate_up_scale,
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I, int E,
@@ -252,7 +263,8 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
   const RoutingTables rt = routing_tables_at(smem);
   const MmaLayout L = mma_layout(H, S);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BK = B * K, nblk = H >> 5, nchunk = H >> 8;
+  constexpr int CB = 64 / NW;  // blocks of 32 columns per chunk
+  const int BK = B * K, nblk = H >> 5, nchunk = nblk / CB;
   const uint32_t base = smem_u32(smem);
   const uint32_t full = base + L.bars, empty = base + L.bars + 8 * kMMaxStages;
   const uint32_t ring = base + L.ring;
@@ -260,7 +272,7 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full + 8 * s, 1);
-      mbar_init(empty + 8 * s, kMWarps);
+      mbar_init(empty + 8 * s, NW);
     }
     mbar_init_fence();
   }
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
   bool ok = enter(c, first_expert(pc, U, lo));
   uint32_t i = 0;
 
-  if (warp == kMWarps) {  // producer
+  if (warp == NW) {  // producer
     if (lane != 0) return;
     const uint32_t bytes = (uint32_t)(2 * L.slab + 32 * nblk);
     for (; ok; ++i, ok = advance(c)) {
@@ -336,7 +348,7 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
 
   // consumers
   const int g = lane >> 2, tig = lane & 3;
-  const uint32_t xs = base + L.xs, red = base + L.red, scl = base + L.scl + 1024 * warp;
+  const uint32_t xs = base + L.xs, red = base + L.red, scl = base + L.scl + 128 * CB * warp;
   int* ktok = reinterpret_cast<int*>(smem + L.ktok);
   const uint8_t* xg = reinterpret_cast<const uint8_t*>(x) + wait_token;
   int staged_u = -1, staged_q = -1, par = 0;
@@ -349,8 +361,8 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
     const int nq = min(xtok, T - c.q * xtok);
     if (c.u != staged_u || c.q != staged_q) {
       // every consumer is past the previous item's barrier: staged x is free
-      stage_x_f16(xs, L.xstride, ktok, xg, sl, nq, H, K);
-      named_barrier_sync(1, kMThreads);
+      stage_x_f16(xs, L.xstride, ktok, xg, sl, nq, H, K, NW);
+      named_barrier_sync(1, 32 * NW);
       staged_u = c.u;
       staged_q = c.q;
     }
@@ -365,8 +377,8 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
       for (int k = 0; k < 4; ++k) acc[r][k] = 0.0f;
     if (!dead) {
       const uint32_t xrow = xs + (uint32_t)((g < nq ? g : 0) * L.xstride + tig * 16);
-      for (int ch = warp; ch < nchunk; ch += kMWarps)
-        mma_chunk(st, H, ch, acc, xrow + (uint32_t)(ch * 512), scl);
+      for (int ch = warp; ch < nchunk; ch += NW)
+        mma_chunk<CB>(st, H, ch, acc, xrow + (uint32_t)(ch * 64 * CB), scl);
       __syncwarp();  // every lane is done with the stage
       if (lane == 0) mbar_arrive(empty + 8 * s);
     }
@@ -377,24 +389,24 @@ __global__ void __launch_bounds__(kMThreads + 32, 1) moe_gate_up_mma(
     const int k1 = (warp < 2 && t0 + 1 < nq) ? ktok[t0 + 1] : 0;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const uint32_t a = red + (uint32_t)((((par * kMWarps + warp) * 2 + r) * 32 + lane) * 16);
+      const uint32_t a = red + (uint32_t)((((par * NW + warp) * 2 + r) * 32 + lane) * 16);
       asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(acc[r][0]),
                    "f"(acc[r][1]), "f"(acc[r][2]), "f"(acc[r][3])
                    : "memory");
     }
-    named_barrier_sync(1, kMThreads);
+    named_barrier_sync(1, 32 * NW);
     if (warp < 2) {  // row tile `warp`: sum the consumer warps' partials
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < kMWarps; ++w) {
-        const uint32_t a = red + (uint32_t)((((par * kMWarps + w) * 2 + warp) * 32 + lane) * 16);
+      for (int w = 0; w < NW; ++w) {
+        const uint32_t a = red + (uint32_t)((((par * NW + w) * 2 + warp) * 32 + lane) * 16);
         const float4 v = lds_f32x4(a);
         sum[0] += v.x;
         sum[1] += v.y;
         sum[2] += v.z;
         sum[3] += v.w;
       }
-      const int n = c.g * kMNeurons + 8 * warp + g;
+      const int n = c.g * kMNeurons + 8 * warp + slab_row(g);
       if (t0 < nq) {
         const float f = exp2_int(-(k0 >> 1)), f2 = exp2_int(-(k0 - (k0 >> 1)));
         const float gv = (sum[0] * f) * f2, uv = (sum[2] * f) * f2;
@@ -427,17 +439,13 @@ bool gate_up_mma_supported(int B, int H, int I, int E, int K) {
          I % kMNeurons == 0 && (long long)E * 2 * I < (1ll << 31) && mma_stages(H) >= 2;
 }
 
-// p.cpl: ring stages (0: the deepest that fits).
-cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                               bool pdl) {
-  if (!gate_up_mma_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
-  int S = mma_stages(a.H);
-  if (p.cpl >= 2 && p.cpl < S) S = p.cpl;
+template <int NW>
+static cudaError_t launch_mma_t(const GateUpArgs& a, int S, cudaStream_t stream, bool pdl) {
   const int smem = mma_layout(a.H, S).total;
   static int configured = 0;
   if (configured < smem) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(moe_gate_up_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t e = cudaFuncSetAttribute(moe_gate_up_mma<NW>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
@@ -449,7 +457,7 @@ cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStr
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(kMThreads + 32);
+  cfg.blockDim = dim3(32 * NW + 32);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -457,9 +465,19 @@ cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gate_up_mma, map, reinterpret_cast<const __nv_bfloat16*>(a.x),
-                            a.topk_ids, a.gate_up_scale, reinterpret_cast<__nv_bfloat16*>(a.h),
-                            a.error_flag, a.B, a.H, a.I, a.E, a.K, S);
+  return cudaLaunchKernelEx(&cfg, moe_gate_up_mma<NW>, map,
+                            reinterpret_cast<const __nv_bfloat16*>(a.x), a.topk_ids,
+                            a.gate_up_scale, reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag,
+                            a.B, a.H, a.I, a.E, a.K, S);
+}
+
+// p.cpl: ring stages (0: the deepest that fits); p.npw: consumer warps (8 or 16).
+cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
+                               bool pdl) {
+  if (!gate_up_mma_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+  int S = mma_stages(a.H);
+  if (p.cpl >= 2 && p.cpl < S) S = p.cpl;
+  return p.npw == 16 ? launch_mma_t<16>(a, S, stream, pdl) : launch_mma_t<8>(a, S, stream, pdl);
 }
 
 }  // namespace wd

@@ -20,6 +20,14 @@ __device__ __forceinline__ uint32_t slab_offset(int row, int col) {
                     (col & 15));
 }
 
+// Which of 8 slab rows MMA tile row g (0..7, the lane's group) reads: tile rows
+// 0..3 take the even rows and 4..7 the odd ones, so that the 16 lanes of a
+// half-warp (tile rows 0..3 or 4..7) read 8-byte pieces of one 32-column block
+// from rows whose swizzle moves them to 8 different 16-byte chunks: the
+// fragment loads are free of bank conflicts (with rows g, the rows g and g^1
+// share a chunk pair and every load took two passes).
+__device__ __forceinline__ int slab_row(int g) { return ((g & 3) << 1) | (g >> 2); }
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
   asm volatile(
@@ -98,6 +106,12 @@ __device__ __forceinline__ int fp16_row_exponent(uint32_t mx) {
 // 2^k for k in [-126, 127].
 __device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
 
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 
 // Host: the driver's tensor-map encoder, looked up once (null if unavailable).
 inline PFN_cuTensorMapEncodeTiled_v12000 mma_tensor_map_encoder() {

@@ -248,6 +248,7 @@ PLANS = [
     "gu=batched:2:1,dn=shared:2",
     "gu=mma,dn=4:1",
     "gu=mma,dn=mma",
+    "gu=mma:2:16,dn=4:1",
     "gu=persist:2:1,dn=mma:2",
 ]
 
@@ -346,10 +347,11 @@ MMA_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("warps", [8, 16])
 @pytest.mark.parametrize("B,H,I,E,K,route", MMA_SHAPES)
-def test_gate_up_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
-    wd.wd_moe_set_plan("gu=mma,dn=4:1")
-    assert "gate_up=moe_gate_up_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
+def test_gate_up_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route, warps):
+    wd.wd_moe_set_plan(f"gu=mma:0:{warps},dn=4:1")
+    assert f"gate_up=moe_gate_up_mma<{warps}," in wd.wd_moe_describe_plan(B, H, I, E, K)
     xs, ids, w, gu, gus, dn, dns = _random_case(900 + B + H + I + E, B, H, I, E, K, route=route)
     check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"gu=mma B={B} H={H} I={I} {route}")
 
