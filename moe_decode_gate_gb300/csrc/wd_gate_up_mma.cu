@@ -88,7 +88,8 @@ struct MmaLayout {
   int xs;       // staged FP16 activations, `xtok` rows of `xstride` bytes
   int xstride;
   int xtok;
-  int ktok;     // per staged token exponent k_t (int[kMTokens])
+  int ktok;     // per staged token exponent k_t (int[kMTokens]), then the
+                // exponents of each partial-sum buffer's item (int[2][kMTokens])
   int red;      // partial sums
   int scl;      // per-warp scale tables
   int total;
@@ -99,16 +100,16 @@ __host__ __device__ inline MmaLayout mma_layout(int H, int S) {
   L.slab = 16 * H;
   L.stage = round_up(2 * L.slab + 2 * 16 * (H / 32), 1024);
   L.bars = kXOffset;
-  L.ring = round_up(kXOffset + 16 * kMMaxStages, 1024);
+  L.ring = round_up(kXOffset + 128, 1024);  // full, empty [kMMaxStages]; rfull, rempty [2]
   L.xs = L.ring + S * L.stage;
   // FP16 row rounded up to 128 bytes, plus 64, so that the two token rows
   // read by one quarter-warp fall in different halves of the 32 banks
   L.xstride = round_up(2 * H, 128) + 64;
-  const int fixed = L.xs + 64 + kMRedBytes + kMScaleBytes;
+  const int fixed = L.xs + 128 + kMRedBytes + kMScaleBytes;
   const int t = (kMSmemCap - fixed) / L.xstride;
   L.xtok = t > kMTokens ? kMTokens : (t < 0 ? 0 : t);
   L.ktok = L.xs + L.xtok * L.xstride;
-  L.red = L.ktok + 64;
+  L.red = L.ktok + 128;
   L.scl = L.red + kMRedBytes;
   L.total = L.scl + kMScaleBytes;
   return L;
@@ -254,7 +255,7 @@ struct MmaCursor {
 // {128, E * 2I, H / 128} with strides {H, 128}, boxes {128, 16, H / 128},
 // 128-byte swizzle.
 template <int NW>
-__global__ void __launch_bounds__(32 * NW + 32, 1) moe_gate_up_mma(
+__global__ void __launch_bounds__(32 * NW + 64, 1) moe_gate_up_mma(
     const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16* __restrict__ x,
     const int32_t* __restrict__ topk_ids, const uint8_t* __restrict__ gate_up_scale,
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I, int E,
@@ -266,13 +267,18 @@ __global__ void __launch_bounds__(32 * NW + 32, 1) moe_gate_up_mma(
   constexpr int CB = 64 / NW;  // blocks of 32 columns per chunk
   const int BK = B * K, nblk = H >> 5, nchunk = nblk / CB;
   const uint32_t base = smem_u32(smem);
-  const uint32_t full = base + L.bars, empty = base + L.bars + 8 * kMMaxStages;
+  const uint32_t full = base + L.bars, empty = full + 8 * kMMaxStages;
+  const uint32_t rfull = empty + 8 * kMMaxStages, rempty = rfull + 16;  // [2] each
   const uint32_t ring = base + L.ring;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full + 8 * s, 1);
       mbar_init(empty + 8 * s, NW);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(rfull + 8 * p, NW);  // each consumer warp's partial sums are in
+      mbar_init(rempty + 8 * p, 1);  // the epilogue warp is done with them
     }
     mbar_init_fence();
   }
@@ -346,21 +352,67 @@ __global__ void __launch_bounds__(32 * NW + 32, 1) moe_gate_up_mma(
     return;
   }
 
+  const uint32_t red = base + L.red;
+  int* ktok = reinterpret_cast<int*>(smem + L.ktok);  // [kMTokens], then rk [2][kMTokens]
+  int* rk = ktok + kMTokens;
+
+  if (warp == NW + 1) {  // epilogue: sums of the consumers' partials, bf16(SiLU(g) * u)
+    const int g = lane >> 2, tig = lane & 3, t0 = 2 * tig;
+    for (; ok; ++i, ok = advance(c)) {
+      const uint32_t p = i & 1;
+      if (!mbar_wait(rfull + 8 * p, (i >> 1) & 1)) {
+        if (lane == 0 && error_flag) atomicOr(error_flag, 2u);
+        break;
+      }
+      const int T = rt.off[c.u + 1] - rt.off[c.u];
+      const int* sl = rt.slots + rt.off[c.u] + c.q * xtok;
+      const int nq = min(xtok, T - c.q * xtok);
+      const int k0 = t0 < nq ? rk[p * kMTokens + t0] : 0;
+      const int k1 = t0 + 1 < nq ? rk[p * kMTokens + t0 + 1] : 0;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float4 v = lds_f32x4(red + (uint32_t)((((p * NW + w) * 2 + r) * 32 + lane) * 16));
+          sum[0] += v.x;
+          sum[1] += v.y;
+          sum[2] += v.z;
+          sum[3] += v.w;
+        }
+        const int n = c.g * kMNeurons + 8 * r + slab_row(g);
+        if (t0 < nq) {
+          const float f = exp2_int(-(k0 >> 1)), f2 = exp2_int(-(k0 - (k0 >> 1)));
+          const float gv = (sum[0] * f) * f2, uv = (sum[2] * f) * f2;
+          h[(size_t)sl[t0] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
+        }
+        if (t0 + 1 < nq) {
+          const float f = exp2_int(-(k1 >> 1)), f2 = exp2_int(-(k1 - (k1 >> 1)));
+          const float gv = (sum[1] * f) * f2, uv = (sum[3] * f) * f2;
+          h[(size_t)sl[t0 + 1] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
+        }
+      }
+      __syncwarp();  // every lane is done with the buffer
+      if (lane == 0) mbar_arrive(rempty + 8 * p);
+    }
+    return;
+  }
+
   // consumers
   const int g = lane >> 2, tig = lane & 3;
-  const uint32_t xs = base + L.xs, red = base + L.red, scl = base + L.scl + 128 * CB * warp;
-  int* ktok = reinterpret_cast<int*>(smem + L.ktok);
+  const uint32_t xs = base + L.xs, scl = base + L.scl + 128 * CB * warp;
   const uint8_t* xg = reinterpret_cast<const uint8_t*>(x) + wait_token;
-  int staged_u = -1, staged_q = -1, par = 0;
+  int staged_u = -1, staged_q = -1;
   bool dead = false;
   for (; ok; ++i, ok = advance(c)) {
-    const uint32_t s = i % S;
+    const uint32_t s = i % S, p = i & 1;
     const uint32_t st = ring + s * L.stage;
     const int T = rt.off[c.u + 1] - rt.off[c.u];
     const int* sl = rt.slots + rt.off[c.u] + c.q * xtok;
     const int nq = min(xtok, T - c.q * xtok);
     if (c.u != staged_u || c.q != staged_q) {
-      // every consumer is past the previous item's barrier: staged x is free
+      // no consumer still reads the previous group's staged x (or its ktok)
+      named_barrier_sync(1, 32 * NW);
       stage_x_f16(xs, L.xstride, ktok, xg, sl, nq, H, K, NW);
       named_barrier_sync(1, 32 * NW);
       staged_u = c.u;
@@ -382,43 +434,22 @@ __global__ void __launch_bounds__(32 * NW + 32, 1) moe_gate_up_mma(
       __syncwarp();  // every lane is done with the stage
       if (lane == 0) mbar_arrive(empty + 8 * s);
     }
-    // this lane's two tokens (read before the barrier: the next item may
-    // restage ktok)
-    const int t0 = 2 * tig;
-    const int k0 = (warp < 2 && t0 < nq) ? ktok[t0] : 0;
-    const int k1 = (warp < 2 && t0 + 1 < nq) ? ktok[t0 + 1] : 0;
+    // partial sums into buffer p, once the epilogue warp is done with it
+    if (!dead && i >= 2 && !mbar_wait(rempty + 8 * p, ((i >> 1) - 1) & 1)) {
+      dead = true;
+      if (lane == 0 && error_flag) atomicOr(error_flag, 2u);
+    }
+    if (dead) continue;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const uint32_t a = red + (uint32_t)((((par * NW + warp) * 2 + r) * 32 + lane) * 16);
+      const uint32_t a = red + (uint32_t)((((p * NW + warp) * 2 + r) * 32 + lane) * 16);
       asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(a), "f"(acc[r][0]),
                    "f"(acc[r][1]), "f"(acc[r][2]), "f"(acc[r][3])
                    : "memory");
     }
-    named_barrier_sync(1, 32 * NW);
-    if (warp < 2) {  // row tile `warp`: sum the consumer warps' partials
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const uint32_t a = red + (uint32_t)((((par * NW + w) * 2 + warp) * 32 + lane) * 16);
-        const float4 v = lds_f32x4(a);
-        sum[0] += v.x;
-        sum[1] += v.y;
-        sum[2] += v.z;
-        sum[3] += v.w;
-      }
-      const int n = c.g * kMNeurons + 8 * warp + slab_row(g);
-      if (t0 < nq) {
-        const float f = exp2_int(-(k0 >> 1)), f2 = exp2_int(-(k0 - (k0 >> 1)));
-        const float gv = (sum[0] * f) * f2, uv = (sum[2] * f) * f2;
-        h[(size_t)sl[t0] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
-      }
-      if (t0 + 1 < nq) {
-        const float f = exp2_int(-(k1 >> 1)), f2 = exp2_int(-(k1 - (k1 >> 1)));
-        const float gv = (sum[1] * f) * f2, uv = (sum[3] * f) * f2;
-        h[(size_t)sl[t0 + 1] * I + n] = __float2bfloat16_rn(silu(gv) * uv);
-      }
-    }
-    par ^= 1;
+    if (warp == 0 && lane < nq) rk[p * kMTokens + lane] = ktok[lane];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rfull + 8 * p);
   }
 }
 
@@ -457,7 +488,7 @@ static cudaError_t launch_mma_t(const GateUpArgs& a, int S, cudaStream_t stream,
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)sms);
-  cfg.blockDim = dim3(32 * NW + 32);
+  cfg.blockDim = dim3(32 * NW + 64);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
