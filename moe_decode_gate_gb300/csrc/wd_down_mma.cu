@@ -13,7 +13,7 @@
 // Organisation:
 //   - grid: one CTA per 16 output dims (H / 16 CTAs); each builds the routing
 //     tables and walks every routed expert in ascending order, in groups of up
-//     to 8 of its (token, slot) pairs; a step is (expert, pair group);
+//     to 4 of its (token, slot) pairs; a step is (expert, pair group);
 //   - a producer warp streams each step into an S-stage ring: the 16 down rows
 //     (16 x I bytes, one 3-D tensor-map copy, 128-byte swizzled so the MMA
 //     fragment reads of 8 rows hit different banks), and, one lane per copy,
@@ -47,10 +47,10 @@ namespace wd {
 namespace {
 
 constexpr int kDWarps = 8;                      // consumer warps
-constexpr int kDConv = 4;                       // converter warps (one per ring stage)
+constexpr int kDConv = 7;                       // converter warps (one per ring stage)
 constexpr int kDThreads = 32 * (kDWarps + 1 + kDConv);
 constexpr int kDRows = 16;                      // output dims per CTA
-constexpr int kDPairs = 8;                      // (token, slot) pairs per step
+constexpr int kDPairs = 4;                      // (token, slot) pairs per step (<= 8)
 constexpr int kDMaxB = 64;                      // tokens (per-warp tables)
 constexpr int kDMaxStages = kDConv;
 constexpr int kDSmemCap = 227 * 1024;
@@ -74,7 +74,7 @@ __host__ __device__ inline DownLayout down_layout(int I, int B, int S) {
   // quarter-warp fall in different halves of the 32 banks
   L.hpitch = d_round(2 * I, 128) + 64;
   L.info = L.hrows + kDPairs * L.hpitch;
-  L.hraw = L.info + kDPairs * 16;
+  L.hraw = L.info + 8 * 16;  // info is read for 8 columns
   L.sraw = L.hraw + kDPairs * 2 * I;
   L.stage = d_round(L.sraw + kDRows * (I / 32), 1024);
   L.bars = kXOffset;  // full, empty, raw (kDMaxStages each)
