@@ -151,7 +151,9 @@ WD_API int wd_moe_launches_per_call(void);
  *   "dn=<output dims per warp>:<blocks per lane per pass>"
  *   "dn=persist:<output dims per warp>:<blocks per lane per pass>"
  *   "dn=stream:<stages>" | "dn=shared:<output dims per CTA>"
- *   "dn=mma[:<ring stages, 2..4>]"  (tensor-core products; B <= 64,
+ *   "dn=3dmma"   (warp per (token, 16 output dims), dots on tensor cores;
+ *                 H % 16 == 0, I % 256 == 0, I <= 1024, K <= 32)
+ *   "dn=mma[:<ring stages, 2..7>]"  (tensor-core products; B <= 64,
  *                                    B*K <= 256, H % 16 == 0, I % 128 == 0)
  *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel
  *                    where the persistent one does not apply>"

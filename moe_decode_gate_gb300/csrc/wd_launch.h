@@ -57,6 +57,7 @@ enum DownVariant {
   kDownPersist = 2,  // moe_down_3d_batched_persist: batched items walked by one wave of CTAs
   kDownShared = 3,   // moe_down_shared: CTA per output-dim group, expert rows shared by tokens
   kDownMma = 4,      // moe_down_mma: CTA per 16 output dims, products by tensor-core MMAs
+  kDown3dMma = 5,    // moe_down_3d_mma: as batched, warp = (token, 16 dims), dots by MMAs
 };
 struct DownPlan {
   int rpw;          // batched, persist: output dims per warp
@@ -100,5 +101,8 @@ cudaError_t launch_down_shared(const DownArgs& a, const DownPlan& p, cudaStream_
 bool down_shared_supported(int B, int H, int I, int E, int K, int rpw);
 cudaError_t launch_down_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_mma_supported(int B, int H, int I, int E, int K);
+cudaError_t launch_down_3d_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream,
+                               bool pdl);
+bool down_3d_mma_supported(int B, int H, int I, int E, int K);
 
 }  // namespace wd

@@ -249,6 +249,8 @@ PLANS = [
     "gu=mma,dn=4:1",
     "gu=mma,dn=mma",
     "gu=mma:2:16,dn=4:1",
+    "gu=mma,dn=3dmma",
+    "gu=batched:2:1,dn=3dmma",
     "gu=persist:2:1,dn=mma:2",
 ]
 
@@ -292,7 +294,8 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
                                   "gu=ring:2,dn=4:1",
                                   "gu=tma,dn=4:1",
                                   "gu=mma,dn=4:1",
-                                  "gu=batched:2:1,dn=mma"])
+                                  "gu=batched:2:1,dn=mma",
+                                  "gu=batched:2:1,dn=3dmma"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
@@ -452,12 +455,13 @@ def _down_alone(dev, h_bits, ids, w, dn, dns, H, E):
     return from_dev_bf16(out), want, int(flag.item())
 
 
-def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset):
+@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma"])
+def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset, plan):
     """h rows are re-encoded per (token, slot) as FP16 times a power of two:
     ordinary rows, rows of magnitude 1e-20 and 1e+20, an all-zero row, BF16
     subnormals only, a row spanning 1e-12 .. 1e+3; a token routed twice to one
     expert and a zero routing weight."""
-    wd.wd_moe_set_plan("dn=mma")
+    wd.wd_moe_set_plan(plan)
     B, H, I, E, K = 6, 256, 256, 4, 3
     xs, ids, w, gu, gus, dn, dns = _random_case(41, B, H, I, E, K)
     ids, w = ids.copy(), w.copy()
@@ -478,10 +482,11 @@ def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset):
         compare(got[t:t + 1], want[t:t + 1], f"dn=mma token {t}")
 
 
-def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset):
+@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma"])
+def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan):
     """E8M0 codes far from 1 (2^-40 .. 2^+19), 0 (2^-127) on a whole row and 255
     (NaN) on one block; an out-of-range id contributes nothing and is flagged."""
-    wd.wd_moe_set_plan("dn=mma")
+    wd.wd_moe_set_plan(plan)
     B, H, I, E, K = 4, 128, 256, 4, 2
     xs, ids, w, gu, gus, dn, dns = _random_case(43, B, H, I, E, K)
     ids = np.array([[0, 1], [1, 2], [0, 9], [2, 3]], dtype=np.int32)
@@ -501,3 +506,30 @@ def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset):
     want[np.isnan(want)] = 0.0
     err = np.abs(got - want).max()
     assert err <= 1e-2 * np.abs(want).max() + 2e-3
+
+
+# moe_down_3d_mma: H % 16 == 0, I % 256 == 0, I <= 1024, K <= 32.  Shapes:
+# the full-size layer at B = 1..64 with every routing pattern, two 16-dim
+# groups (H = 32), I = 1024 (four 8-block passes per routed row) and I = 256
+# (one), and K == E.
+DN_3DMMA_SHAPES = [
+    (1, 2048, 768, 128, 8, "uniform"),
+    (8, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "uniform"),
+    (32, 2048, 768, 128, 8, "zipf"),
+    (32, 2048, 768, 128, 8, "fixed"),
+    (32, 2048, 768, 128, 8, "disjoint"),
+    (64, 2048, 768, 128, 4, "uniform"),
+    (5, 32, 512, 4, 2, "uniform"),
+    (7, 2048, 1024, 6, 6, "uniform"),
+    (6, 256, 256, 5, 1, "uniform"),
+    (3, 512, 256, 3, 3, "uniform"),
+]
+
+
+@pytest.mark.parametrize("B,H,I,E,K,route", DN_3DMMA_SHAPES)
+def test_down_3d_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
+    wd.wd_moe_set_plan("dn=3dmma")
+    assert "down=moe_down_3d_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
+    xs, ids, w, gu, gus, dn, dns = _random_case(1300 + B + H + I + E, B, H, I, E, K, route=route)
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"dn=3dmma B={B} H={H} I={I} {route}")
