@@ -58,9 +58,10 @@ constexpr int kDSmemCap = 227 * 1024;
 __host__ __device__ constexpr int d_round(int v, int a) { return (v + a - 1) / a * a; }
 
 // Stage: [0, 16 I) swizzled down rows; FP32 scales [16 rows][I/32 blocks];
-// FP16 h rows [8 pairs][hpitch]; pair info [8] x {float w, int k, int token,
-// 0}; then what the copies bring for the converter: the pairs' BF16 h rows
-// [8][2 I] and the rows' scale codes [16][I/32].
+// FP16 h rows [kDPairs][hpitch]; pair info [8] x {float w, int k, int token,
+// 0} (read for all 8 MMA columns, filled for the step's pairs); then what the
+// copies bring for the converter: the pairs' BF16 h rows [kDPairs][2 I] and the
+// rows' scale codes [16][I/32].
 struct DownLayout {
   int scales, hrows, hpitch, info, hraw, sraw, stage;
   int bars, ring, tables, total;

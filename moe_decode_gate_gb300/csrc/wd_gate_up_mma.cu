@@ -30,9 +30,15 @@
 //     reads of 8 rows hit different banks) and their scale bytes (two bulk
 //     copies of 16 x H/32 bytes).  The bytes in flight are held by shared
 //     memory (two items, 130 KiB per SM at H = 2048), not by registers;
-//   - 8 consumer warps split H: warp w owns the 256-column chunks w, w+8, ...
-//     of the item.  Their partial accumulators are summed through shared
-//     memory (one named barrier per item); the epilogue is lane-local;
+//   - the consumer warps (8, or 16 on request) split H: at H = 2048 each owns
+//     one 256-column (128-column) chunk of every item.  They write their
+//     partial tiles into one of two shared-memory buffers guarded by mbarriers
+//     and go on; an epilogue warp sums each buffer and stores the item's
+//     bf16(SiLU(g) * u) values (gate and up of one output sit in one lane).
+//     The consumers meet at a named barrier only when the staged activations
+//     change;
+//   - MMA tile row g reads slab row 2 (g % 4) + g / 4, which keeps every
+//     half-warp's fragment loads on 8 distinct swizzled 16-byte chunks;
 //   - MXFP8 block scales: the two k16 MMAs of one 32-column block accumulate
 //     into a fresh tile, which is then multiplied by the block's power-of-two
 //     scale into the running FP32 sum (exact barring FP32 over/underflow);
@@ -54,8 +60,9 @@
 //
 // Every mbarrier wait is bounded (wd_pipeline.cuh).  A consumer whose wait
 // runs out raises bit 1 of the error flag and computes nothing more but keeps
-// following the consumers' barriers; the producer stops issuing when its wait
-// runs out, and before exiting waits (bounded) for the copies it issued last.
+// following the consumers' barriers; the epilogue warp stops at its first wait
+// that runs out; the producer stops issuing when its wait runs out, and before
+// exiting waits (bounded) for the copies it issued last.
 #include "wd_launch.h"
 #include "wd_mma.cuh"
 #include "wd_persist.cuh"
