@@ -207,12 +207,25 @@ __device__ __forceinline__ void mma_chunk(uint32_t st, int H, int c, float (&acc
     code[0] = lds_u32(sc + lane * nblk + c * CB);
   }
   __syncwarp();  // the previous chunk's scale reads are done
+  // codes 1..254 decode as code << 23; a lane holding a 0 (2^-127) or 255
+  // (NaN) takes the general rule
+  bool special = false;
 #pragma unroll
-  for (int q = 0; q < CB / 4; ++q)
+  for (int q = 0; q < CB / 4; ++q) special |= e8m0x4_any_special(code[q]);
+#pragma unroll
+  for (int q = 0; q < CB / 4; ++q) {
+    float f[4];
+    if (!special) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) f[t] = __uint_as_float(((code[q] >> (8 * t)) & 0xFFu) << 23);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) f[t] = e8m0_to_f32((code[q] >> (8 * t)) & 0xFFu);
+    }
     asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(scl + 4 * CB * lane + 16 * q),
-                 "f"(e8m0_to_f32(code[q] & 0xFFu)), "f"(e8m0_to_f32((code[q] >> 8) & 0xFFu)),
-                 "f"(e8m0_to_f32((code[q] >> 16) & 0xFFu)), "f"(e8m0_to_f32(code[q] >> 24))
+                 "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3])
                  : "memory");
+  }
   __syncwarp();
   float4 sg4[2], su4[2];
 #pragma unroll

@@ -107,6 +107,13 @@ __device__ __forceinline__ int fp16_row_exponent(uint32_t mx) {
 __device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
 
 
+// True if any byte of w is an E8M0 code whose 8 bits are all equal: 0x00
+// (2^-127) or 0xFF (NaN), the two codes that do not decode as code << 23.
+__device__ __forceinline__ bool e8m0x4_any_special(uint32_t w) {
+  const uint32_t d = (w ^ (w >> 1)) & 0x7F7F7F7Fu;  // per byte: 0 iff all 8 bits are equal
+  return ((d + 0x7F7F7F7Fu) & 0x80808080u) != 0x80808080u;
+}
+
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
