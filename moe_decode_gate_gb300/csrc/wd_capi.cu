@@ -25,7 +25,7 @@ namespace wd {
 //   "gu=mixed:<npw>:<stages>" | "gu=persist:<npw>:<prefetch+1>" | "gu=ring:<stages>" | "gu=tma" |
 //   "gu=mma[:<stages>[:<consumer warps, 8 or 16>]]",
 //   "dn=<rpw>:<qpl>" | "dn=stream:<stages>" | "dn=persist:<rpw>:<qpl>" | "dn=shared:<rpw>" |
-//   "dn=mma[:<stages>]" | "dn=3dmma",
+//   "dn=mma[:<stages>]" | "dn=3dmma" | "dn=emma[:<stages>[:<parts of I, 1 or 2>]]",
 //   "rowshare_min_b=<B>", "pdl=<mask>" (bit 0: the gate/up launch may overlap the
 //   kernel before it, bit 1: the down launch may overlap gate/up), comma-separated;
 //   "" or NULL restores the defaults.
@@ -90,6 +90,18 @@ bool parse_plan(const char* spec, PlanOverride* out) {
       } else if (sscanf(tok, "dn=mma:%d", &a) == 1) {
         p.dn_variant = kDownMma;
         p.dn_qpl = a;
+      } else if (sscanf(tok, "dn=emma:%d:%d", &a, &b) == 2) {
+        p.dn_variant = kDownExpertMma;
+        p.dn_qpl = a;
+        p.dn_rpw = b;
+      } else if (sscanf(tok, "dn=emma:%d", &a) == 1) {
+        p.dn_variant = kDownExpertMma;
+        p.dn_qpl = a;
+        p.dn_rpw = 1;
+      } else if (strcmp(tok, "dn=emma") == 0) {
+        p.dn_variant = kDownExpertMma;
+        p.dn_qpl = 0;
+        p.dn_rpw = 1;
       } else if (strcmp(tok, "dn=3dmma") == 0) {
         p.dn_variant = kDown3dMma;
       } else if (strcmp(tok, "dn=mma") == 0) {
@@ -174,6 +186,8 @@ DownPlan plan_down(int B, int H, int I, int K, int E) {
     return DownPlan{16, o.dn_qpl, kDownMma};
   if (o.dn_variant == kDown3dMma && down_3d_mma_supported(B, H, I, E, K))
     return DownPlan{16, 0, kDown3dMma};
+  if (o.dn_variant == kDownExpertMma && down_expert_mma_supported(B, H, I, E, K))
+    return DownPlan{o.dn_rpw == 2 ? 2 : 1, o.dn_qpl, kDownExpertMma};
   if (B >= 4) return DownPlan{4, 1, kDownBatched};  // 4 output dims share each h block
   const int nq = K * (I / 32);
   const int per_lane = (nq + 31) / 32;
@@ -208,7 +222,7 @@ GateUpPlan plan_gate_up_for(const GateUpArgs& a) {
 DownPlan plan_down_for(const DownArgs& a) {
   DownPlan p = plan_down(a.B, a.H, a.I, a.K, a.E);
   if ((p.variant == kDownStream && !(aligned16(a.down) && aligned16(a.down_scale))) ||
-      ((p.variant == kDownMma || p.variant == kDown3dMma) &&
+      ((p.variant == kDownMma || p.variant == kDown3dMma || p.variant == kDownExpertMma) &&
        !(aligned16(a.down) && aligned16(a.down_scale) && aligned16(a.h)))) {
     const int per_lane = (a.K * (a.I / 32) + 31) / 32;
     p = DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
@@ -366,9 +380,10 @@ wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, siz
                                          "moe_gate_up_tma", "moe_gate_up_mma"};
   static const char* const dn_names[] = {"moe_down_3d_batched", "moe_down_stream",
                                          "moe_down_3d_batched_persist", "moe_down_shared",
-                                         "moe_down_mma", "moe_down_3d_mma"};
+                                         "moe_down_mma", "moe_down_3d_mma",
+                                         "moe_down_expert_mma"};
   const char* gn = (g.variant >= 0 && g.variant <= 7) ? gu_names[g.variant] : "?";
-  const char* dn = (d.variant >= 0 && d.variant <= 5) ? dn_names[d.variant] : "?";
+  const char* dn = (d.variant >= 0 && d.variant <= 6) ? dn_names[d.variant] : "?";
   snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d> pdl=%d", gn, g.npw, g.cpl, dn, d.rpw,
            d.qpl, wd::pdl_mask_for(g));
   return WD_OK;

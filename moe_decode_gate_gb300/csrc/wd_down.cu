@@ -285,6 +285,7 @@ cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t strea
   if (p.variant == kDownShared) return launch_down_shared(a, p, stream, pdl);
   if (p.variant == kDownMma) return launch_down_mma(a, p, stream, pdl);
   if (p.variant == kDown3dMma) return launch_down_3d_mma(a, p, stream, pdl);
+  if (p.variant == kDownExpertMma) return launch_down_expert_mma(a, p, stream, pdl);
   if (p.variant == kDownPersist) {
     if (p.rpw == 4 && p.qpl == 1) return launch_down_persist_t<4, 1>(a, stream, pdl);
     if (p.rpw == 2 && p.qpl == 1) return launch_down_persist_t<2, 1>(a, stream, pdl);

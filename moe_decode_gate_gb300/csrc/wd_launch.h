@@ -58,6 +58,7 @@ enum DownVariant {
   kDownShared = 3,   // moe_down_shared: CTA per output-dim group, expert rows shared by tokens
   kDownMma = 4,      // moe_down_mma: CTA per 16 output dims, products by tensor-core MMAs
   kDown3dMma = 5,    // moe_down_3d_mma: as batched, warp = (token, 16 dims), dots by MMAs
+  kDownExpertMma = 6,  // moe_down_expert_mma: CTA per 16 output dims, warp per routed-expert step
 };
 struct DownPlan {
   int rpw;          // batched, persist: output dims per warp
@@ -104,5 +105,8 @@ bool down_mma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down_3d_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream,
                                bool pdl);
 bool down_3d_mma_supported(int B, int H, int I, int E, int K);
+cudaError_t launch_down_expert_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream,
+                                   bool pdl);
+bool down_expert_mma_supported(int B, int H, int I, int E, int K);
 
 }  // namespace wd

@@ -136,14 +136,17 @@ inline PFN_cuTensorMapEncodeTiled_v12000 mma_tensor_map_encoder() {
 
 // Host: a row-major byte matrix [rows][cols] (cols a multiple of 128) as the
 // 3-D tensor {128, rows, cols/128} with strides {cols, 128}, so that one box
-// {128, 16, cols/128} is 16 whole rows, stored in shared memory as
-// [cols/128][16][128] with the 128-byte swizzle (slab_offset).
-inline bool encode_row_slab_map(CUtensorMap* map, const void* base, uint64_t rows, int cols) {
+// {128, 16, box_cols/128} is box_cols columns of 16 rows (whole rows when
+// box_cols is 0 or cols), stored in shared memory as [box_cols/128][16][128]
+// with the 128-byte swizzle (slab_offset).
+inline bool encode_row_slab_map(CUtensorMap* map, const void* base, uint64_t rows, int cols,
+                                int box_cols = 0) {
+  if (box_cols <= 0) box_cols = cols;
   PFN_cuTensorMapEncodeTiled_v12000 enc = mma_tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {128, rows, (cuuint64_t)(cols / 128)};
   const cuuint64_t strides[2] = {(cuuint64_t)cols, 128};
-  const cuuint32_t box[3] = {128, 16, (cuuint32_t)(cols / 128)};
+  const cuuint32_t box[3] = {128, 16, (cuuint32_t)(box_cols / 128)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

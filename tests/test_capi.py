@@ -149,6 +149,12 @@ def test_built_in_plan_by_batch():
     assert wd.wd_moe_describe_plan(32, 4096, 768, 128, 8).startswith("gate_up=moe_gate_up_persist<2,1>")
     # B*K above the persistent kernel's routing tables: the shared-row kernel
     assert wd.wd_moe_describe_plan(64, **q).startswith("gate_up=moe_gate_up_rowshare<2,2>")
+    wd.wd_moe_set_plan("gu=mma,dn=emma:12")
+    try:
+        assert wd.wd_moe_describe_plan(32, **q) == \
+            "gate_up=moe_gate_up_mma<8,0> down=moe_down_expert_mma<1,12> pdl=1"
+    finally:
+        wd.wd_moe_set_plan(None)
     wd.wd_moe_set_plan("gu=batched:1:2,dn=shared:4")
     try:
         assert wd.wd_moe_describe_plan(32, **q) == \
@@ -172,6 +178,9 @@ def test_plan_override_parser():
     assert lib.wd_moe_set_plan(b"gu=ring:2") == OK
     assert lib.wd_moe_set_plan(b"gu=mma,pdl=3") == OK
     assert lib.wd_moe_set_plan(b"gu=mma:2,pdl=0") == OK
+    assert lib.wd_moe_set_plan(b"gu=mma,dn=emma") == OK
+    assert lib.wd_moe_set_plan(b"dn=emma:3,pdl=3") == OK
+    assert lib.wd_moe_set_plan(b"dn=emma:0:2") == OK
     assert lib.wd_moe_set_plan(b"pdl=4") == INVALID
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID

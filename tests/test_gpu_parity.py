@@ -252,6 +252,9 @@ PLANS = [
     "gu=mma,dn=3dmma",
     "gu=batched:2:1,dn=3dmma",
     "gu=persist:2:1,dn=mma:2",
+    "gu=mma,dn=emma",
+    "gu=persist:2:1,dn=emma:8",
+    "gu=mma,dn=emma:0:2",
 ]
 
 PLAN_SHAPES = [
@@ -295,7 +298,8 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
                                   "gu=tma,dn=4:1",
                                   "gu=mma,dn=4:1",
                                   "gu=batched:2:1,dn=mma",
-                                  "gu=batched:2:1,dn=3dmma"])
+                                  "gu=batched:2:1,dn=3dmma",
+                                  "gu=batched:2:1,dn=emma"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
@@ -436,12 +440,15 @@ DN_MMA_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("plan,kernel", [("dn=mma", "moe_down_mma<"),
+                                         ("dn=emma", "moe_down_expert_mma<"),
+                                         ("dn=emma:0:2", "moe_down_expert_mma<")])
 @pytest.mark.parametrize("B,H,I,E,K,route", DN_MMA_SHAPES)
-def test_down_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
-    wd.wd_moe_set_plan("dn=mma")
-    assert "down=moe_down_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
+def test_down_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route, plan, kernel):
+    wd.wd_moe_set_plan(plan)
+    assert f"down={kernel}" in wd.wd_moe_describe_plan(B, H, I, E, K)
     xs, ids, w, gu, gus, dn, dns = _random_case(1100 + B + H + I + E, B, H, I, E, K, route=route)
-    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"dn=mma B={B} H={H} I={I} {route}")
+    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"{plan} B={B} H={H} I={I} {route}")
 
 
 def _down_alone(dev, h_bits, ids, w, dn, dns, H, E):
@@ -455,7 +462,7 @@ def _down_alone(dev, h_bits, ids, w, dn, dns, H, E):
     return from_dev_bf16(out), want, int(flag.item())
 
 
-@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma"])
+@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma", "dn=emma"])
 def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset, plan):
     """h rows are re-encoded per (token, slot) as FP16 times a power of two:
     ordinary rows, rows of magnitude 1e-20 and 1e+20, an all-zero row, BF16
@@ -479,10 +486,10 @@ def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset, plan):
     got, want, flag = _down_alone(cuda_device, hb, ids, w, dn, dns, H, E)
     assert flag == 0
     for t in range(B):  # per token: the rows differ by up to 40 orders of magnitude
-        compare(got[t:t + 1], want[t:t + 1], f"dn=mma token {t}")
+        compare(got[t:t + 1], want[t:t + 1], f"{plan} token {t}")
 
 
-@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma"])
+@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma", "dn=emma"])
 def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan):
     """E8M0 codes far from 1 (2^-40 .. 2^+19), 0 (2^-127) on a whole row and 255
     (NaN) on one block; an out-of-range id contributes nothing and is flagged."""
