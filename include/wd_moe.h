@@ -155,6 +155,11 @@ WD_API int wd_moe_launches_per_call(void);
  *                 H % 16 == 0, I % 256 == 0, I <= 1024, K <= 32)
  *   "dn=mma[:<ring stages, 2..7>]"  (tensor-core products; B <= 64,
  *                                    B*K <= 256, H % 16 == 0, I % 128 == 0)
+ *   "dn=emma[:<ring stages, 8..16>[:<parts of I per step, 1 or 2>]]"
+ *                (tensor-core products, one warp per routed-expert step;
+ *                 B <= 64, B*K <= 256, H % 16 == 0, I % 128 == 0, and a
+ *                 ring of 8 stages fitting in shared memory: any such B up
+ *                 to I = 768, small B up to I = 1024)
  *   "rowshare_min_b=<smallest batch that uses the shared-row gate/up kernel
  *                    where the persistent one does not apply>"
  *   "pdl=<0..3>" (programmatic dependent launch: bit 0 lets the gate/up
