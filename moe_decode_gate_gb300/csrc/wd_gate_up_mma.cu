@@ -27,8 +27,10 @@
 //     into an S-stage shared-memory ring with four copies that complete on the
 //     stage's mbarrier: the 16 gate rows and the 16 up rows (each one 3-D
 //     tensor-map copy, 16 x H bytes, 128-byte swizzled so that the MMA fragment
-//     reads of 8 rows hit different banks) and their scale bytes (two bulk
-//     copies of 16 x H/32 bytes).  The bytes in flight are held by shared
+//     reads of 8 rows hit different banks) and their scale bytes (two 3-D
+//     tensor-map copies of 16 x H/32 bytes, stored as [H/512][16 rows][16] so
+//     that the 8 or 4 codes a lane reads for its row and chunk sit 16 bytes
+//     from the next row's, not H/32).  The bytes in flight are held by shared
 //     memory (two items, 130 KiB per SM at H = 2048), not by registers;
 //   - the consumer warps (8, or 16 on request) split H: at H = 2048 each owns
 //     one 256-column (128-column) chunk of every item.  They write their
@@ -197,14 +199,16 @@ __device__ __forceinline__ void mma_chunk(uint32_t st, int H, int c, float (&acc
   const int nblk = H >> 5;
   const uint32_t gate = st, up = st + 16 * H, sc = st + 32 * H;
   // lane l decodes table row l (gate rows 0..15, then up rows 0..15), blocks
-  // CB c .. CB c + CB - 1
+  // CB c .. CB c + CB - 1: codes [16-block group][row][16] per 16-row half
+  const int o = c * CB;
+  const uint32_t src = sc + (uint32_t)((lane >> 4) * 16 * nblk + (o >> 4) * 256 + (lane & 15) * 16 + (o & 15));
   uint32_t code[CB / 4];
   if (CB == 8) {
-    const uint2 v = lds_u32x2(sc + lane * nblk + c * CB);
+    const uint2 v = lds_u32x2(src);
     code[0] = v.x;
     code[CB / 4 - 1] = v.y;
   } else {
-    code[0] = lds_u32(sc + lane * nblk + c * CB);
+    code[0] = lds_u32(src);
   }
   __syncwarp();  // the previous chunk's scale reads are done
   // codes 1..254 decode as code << 23; a lane holding a 0 (2^-127) or 255
@@ -273,11 +277,12 @@ struct MmaCursor {
 // item: 8 warps x 256 or 16 warps x 128 at H = 2048), then one producer warp.
 // `S`: ring stages.  `tmap`: the gate/up codes as a 3-D byte tensor
 // {128, E * 2I, H / 128} with strides {H, 128}, boxes {128, 16, H / 128},
-// 128-byte swizzle.
+// 128-byte swizzle.  `smap`: their scale codes as a 3-D byte tensor
+// {16, E * 2I, H / 512} with strides {H / 32, 16}, boxes {16, 16, H / 512}.
 template <int NW>
 __global__ void __launch_bounds__(32 * NW + 64, 1) moe_gate_up_mma(
-    const __grid_constant__ CUtensorMap tmap, const __nv_bfloat16* __restrict__ x,
-    const int32_t* __restrict__ topk_ids, const uint8_t* __restrict__ gate_up_scale,
+    const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap smap,
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_ids,
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I, int E,
     int K, int S) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -361,10 +366,8 @@ __global__ void __launch_bounds__(32 * NW + 64, 1) moe_gate_up_mma(
       const int row0 = rt.expert[c.u] * 2 * I + c.g * kMNeurons;  // < 2^31 (checked on launch)
       tma_load_3d(st, &tmap, 0, row0, 0, full + 8 * s);
       tma_load_3d(st + L.slab, &tmap, 0, row0 + I, 0, full + 8 * s);
-      bulk_g2s_nohint(st + 2 * L.slab, gate_up_scale + (size_t)row0 * nblk, (uint32_t)(16 * nblk),
-                      full + 8 * s);
-      bulk_g2s_nohint(st + 2 * L.slab + 16 * nblk, gate_up_scale + (size_t)(row0 + I) * nblk,
-                      (uint32_t)(16 * nblk), full + 8 * s);
+      tma_load_3d(st + 2 * L.slab, &smap, 0, row0, 0, full + 8 * s);
+      tma_load_3d(st + 2 * L.slab + 16 * nblk, &smap, 0, row0 + I, 0, full + 8 * s);
     }
     // the copies issued last land before the CTA exits
     for (uint32_t k = i > (uint32_t)S ? i - S : 0u; k < i; ++k)
@@ -500,8 +503,9 @@ static cudaError_t launch_mma_t(const GateUpArgs& a, int S, cudaStream_t stream,
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  CUtensorMap map;
-  if (!encode_row_slab_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H))
+  CUtensorMap map, smap;
+  if (!encode_row_slab_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H) ||
+      !encode_scale_group_map(&smap, a.gate_up_scale, (uint64_t)a.E * 2 * a.I, a.H / 32))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -516,9 +520,9 @@ static cudaError_t launch_mma_t(const GateUpArgs& a, int S, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_gate_up_mma<NW>, map,
+  return cudaLaunchKernelEx(&cfg, moe_gate_up_mma<NW>, map, smap,
                             reinterpret_cast<const __nv_bfloat16*>(a.x), a.topk_ids,
-                            a.gate_up_scale, reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag,
+                            reinterpret_cast<__nv_bfloat16*>(a.h), a.error_flag,
                             a.B, a.H, a.I, a.E, a.K, S);
 }
 

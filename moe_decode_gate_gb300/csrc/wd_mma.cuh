@@ -153,5 +153,20 @@ inline bool encode_row_slab_map(CUtensorMap* map, const void* base, uint64_t row
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Host: a row-major byte matrix [rows][cols] (cols a multiple of 16) as the
+// 3-D tensor {16, rows, cols/16} with strides {cols, 16}, so that one box
+// {16, 16, cols/16} is 16 whole rows stored in shared memory as
+// [cols/16][16][16]: the 16-byte groups of consecutive rows are adjacent.
+inline bool encode_scale_group_map(CUtensorMap* map, const void* base, uint64_t rows, int cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = mma_tensor_map_encoder();
+  if (!enc || cols % 16 != 0 || cols / 16 > 256) return false;
+  const cuuint64_t dims[3] = {16, rows, (cuuint64_t)(cols / 16)};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols, 16};
+  const cuuint32_t box[3] = {16, 16, (cuuint32_t)(cols / 16)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace wd
