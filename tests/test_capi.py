@@ -155,6 +155,13 @@ def test_built_in_plan_by_batch():
             "gate_up=moe_gate_up_mma<8,0> down=moe_down_expert_mma<1,12> pdl=1"
     finally:
         wd.wd_moe_set_plan(None)
+    # a shape the expert-step down kernel does not take (B > 64) keeps the built-in down
+    wd.wd_moe_set_plan("dn=emma")
+    try:
+        assert wd.wd_moe_describe_plan(32, **q).endswith("down=moe_down_expert_mma<1,0> pdl=1")
+        assert "down=moe_down_3d_batched<4,1>" in wd.wd_moe_describe_plan(128, 2048, 768, 128, 2)
+    finally:
+        wd.wd_moe_set_plan(None)
     wd.wd_moe_set_plan("gu=batched:1:2,dn=shared:4")
     try:
         assert wd.wd_moe_describe_plan(32, **q) == \
