@@ -6,13 +6,26 @@ layers with the Qwen-3-style shapes H=2048, I=768, E=128, K=8, each layer with
 its own seeded MXFP8 weights (604 MB per layer, 29 GB in all, far above L2);
 the BF16 output of layer l is the input of layer l+1; router outputs are the
 seeded top-8 of N(0,1) logits per layer.  One step = one token-step of B
-tokens through all 48 layers (96 kernel launches, replayed as a CUDA graph).
+tokens through all 48 layers (2 or 3 launches per layer, replayed as one CUDA
+graph).
 
 Reported metric: achieved HBM GB/s = exact algorithmic bytes of the step
 (each distinct routed expert's weights and scales once per layer, plus x, the
 intermediate h written and read, out, ids and weights) / step time; also
-us/layer and the fraction of the copy-kernel bandwidth this bench measures
-itself.  The headline line is B=32; the sweep B in {1,2,4,8,16,32} rides along.
+us/layer and the fraction of the largest copy bandwidth measured on this GPU
+(this bench's own copy kernel, torch's copy, and the measured peak).
+The headline line is B=32; alongside it:
+  - the B-sweep of the stack (B = 1..32) with the plan each B runs, and at
+    B = 8..32 the pages' own two-kernel form and the previous default plan;
+  - single layers of the other workloads (one Qwen-3-style layer at B=1, the
+    B-sweep layer, the three routing-stress layers at B=32), each timed cold
+    (L2 flushed before every timed call);
+  - the stack with fresh activations at every layer (timing only: the chained
+    stack's activations collapse to zero after a few layers);
+  - each kernel of the plan timed alone, and the roofline of the one that
+    takes longest per launch;
+  - the same step end to end through the public API with host buffers;
+  - the FP64 CPU oracle on one host core and on all of them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -22,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -40,26 +54,42 @@ METRIC = "MoE decode layer HBM GB/s and us/layer at B=1-32, % of measured copy p
 UNIT = "GB/s"
 HEADLINE_B = 32
 SWEEP_B = (1, 2, 4, 8, 16, 32)
+# plans timed beside the built-in one on the stack (B >= 8, where they differ)
+COMPARE_PLANS = {
+    "pages_form": "gu=batched:2:1,dn=4:1",   # the pages' two kernels at every B
+    "per_token_down": "gu=mma,dn=4:1,pdl=1",  # shared-row gate/up, per-(token, dims) down
+}
+L2_FLUSH_BYTES = 512 << 20  # written before every cold single-layer call (L2 is 126 MB)
 
 
 # ------------------------------------------------------------------ helpers --
-
-def algorithmic_bytes(ids_layers, B, H, I, E, K):
-    """Exact bytes one step must move: per layer, every distinct routed expert's
-    codes + scales once, x read, h written and read, out written, ids + w read."""
-    per_layer_act = 2 * B * H + 2 * 2 * B * K * I + 2 * B * H + 8 * B * K
-    wbytes = sum(synth.unique_expert_bytes(ids, E, H, I) for ids in ids_layers)
-    return wbytes + per_layer_act * len(ids_layers)
-
 
 def gate_up_bytes(ids, B, H, I, E, K):
     uniq = np.unique(ids[(ids >= 0) & (ids < E)]).size
     return uniq * (2 * I * H + 2 * I * H // 32) + 2 * B * H + 2 * B * K * I + 4 * B * K
 
 
+def encode_bytes(B, I, K):
+    """moe_h_encode: h read, its FP16 copy written, one exponent per row."""
+    return 2 * B * K * I + 2 * B * K * I + 4 * B * K
+
+
 def down_bytes(ids, B, H, I, E, K):
+    """Either down kernel: the routed experts' rows once, h (or its FP16 copy)
+    once, out, ids and weights (+ the per-row exponents, 4 bytes a row)."""
     uniq = np.unique(ids[(ids >= 0) & (ids < E)]).size
     return uniq * (H * I + H * I // 32) + 2 * B * K * I + 2 * B * H + 8 * B * K
+
+
+def layer_bytes(ids, B, H, I, E, K):
+    """Algorithmic bytes of one layer: gate/up + down as the pages' two
+    kernels move them (the encode pass of the shared-row down is not counted:
+    it is this implementation's choice, not the method's traffic)."""
+    return gate_up_bytes(ids, B, H, I, E, K) + down_bytes(ids, B, H, I, E, K)
+
+
+def algorithmic_bytes(ids_layers, B, H, I, E, K):
+    return sum(layer_bytes(ids, B, H, I, E, K) for ids in ids_layers)
 
 
 def read_peaks_file():
@@ -82,9 +112,11 @@ def kernel_sources_sha():
     return h.hexdigest()[:16]
 
 
-def profile_traffic(kernel):
-    """dram bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def profile_traffic(kernel, mean_alg_bytes):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources, scaled from the profiled launch to a launch
+    with the mean algorithmic bytes (dram / algorithmic of the SAME profiled
+    launch, times the mean); else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
@@ -93,7 +125,11 @@ def profile_traffic(kernel):
     if d.get("sources_sha") != kernel_sources_sha():
         return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch_full")
+    if not k or not k.get("algorithmic_bytes_profiled_launch"):
+        return None
+    ratio = k["dram_bytes_profiled_launch"] / k["algorithmic_bytes_profiled_launch"]
+    return {"bytes_per_launch": round(ratio * mean_alg_bytes), "dram_over_algorithmic": round(ratio, 4),
+            "profiled": k.get("profiled", "")}
 
 
 class ClockSampler:
@@ -154,7 +190,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def plan_of(wd, B, H, I, E, K):
+    """{"gate_up": ..., "down": ..., "pdl": ..., "launches": ...} of the current plan."""
+    return dict(kv.split("=", 1) for kv in wd.wd_moe_describe_plan(B, H, I, E, K).split())
+
+
 # ----------------------------------------------------------- the GPU stack --
+
+def upload_layer(torch, dev, wl, layer):
+    gu, gus = synth.gate_up(wl.seed, layer, wl.E, wl.H, wl.I)
+    dn, dns = synth.down(wl.seed, layer, wl.E, wl.H, wl.I)
+    return tuple(torch.from_numpy(a).to(dev) for a in (gu, gus, dn, dns))
+
 
 class Stack:
     """48 layers of device-resident MXFP8 weights plus per-B routing and buffers."""
@@ -190,18 +237,26 @@ class Stack:
             ws.append(w)
         return np.stack(ids), np.stack(ws)
 
-    def buffers(self, B):
+    def buffers(self, B, fresh_inputs=False):
+        """Routing and activations of a step at batch B.  fresh_inputs: every
+        layer reads its own seeded N(0,1) activations instead of the previous
+        layer's output (timing only)."""
         torch = self.torch
         ids, ws = self.routing(B)
         xs = synth.x(WORKLOAD.seed, 0, B, self.H)
-        d = dict(B=B, ids_host=ids, w_host=ws, x_host=xs)
+        d = dict(B=B, ids_host=ids, w_host=ws, x_host=xs, fresh=fresh_inputs)
         d["ids"] = torch.from_numpy(ids).to(self.dev)
         d["w"] = torch.from_numpy(ws).to(self.dev)
         d["x0"] = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(self.dev)
         d["act"] = [torch.empty((B, self.H), dtype=torch.bfloat16, device=self.dev) for _ in range(2)]
+        if fresh_inputs:
+            xl = np.stack([synth.x(WORKLOAD.seed, l, B, self.H) for l in range(self.L)])
+            d["x_layers"] = torch.from_numpy(xl.view(np.int16)).view(torch.bfloat16).to(self.dev)
         return d
 
     def layer_io(self, buf, l):
+        if buf.get("fresh"):
+            return buf["x_layers"][l], buf["act"][l % 2]
         x = buf["x0"] if l == 0 else buf["act"][(l - 1) % 2]
         return x, buf["act"][l % 2]
 
@@ -227,6 +282,9 @@ class Stack:
             self.enqueue_step(buf, stream=s)
         return g, s
 
+    def launches_per_step(self, B):
+        return self.L * self.wd.wd_moe_launches(B, self.H, self.I, self.E, self.K)
+
 
 def time_graph(torch, dev, g, s, steps, warmup, barrier):
     for _ in range(warmup):
@@ -246,66 +304,93 @@ def time_graph(torch, dev, g, s, steps, warmup, barrier):
 
 
 def time_kernels_alone(torch, wd, dev, stack, buf, steps):
-    """Per-launch device time of each kernel on its own (no overlap), events on
-    the launching stream around every launch; weights are cold (48 layers)."""
-    B, K, I, H = buf["B"], stack.K, stack.I, stack.H
+    """Per-launch device time of each kernel of the plan on its own (no
+    overlap), CUDA events on the launching stream around every launch; weights
+    are cold (48 layers between two uses).  Returns {kernel: {...}}."""
+    B, K, I, H, E = buf["B"], stack.K, stack.I, stack.H, stack.E
+    plan = plan_of(wd, B, H, I, E, K)
+    shared_down = plan["down"].startswith("moe_down_dimblock")
     s = torch.cuda.Stream(device=dev)
     h = torch.empty((B, K, I), dtype=torch.bfloat16, device=dev)
+    h16 = torch.empty((B, K, I), dtype=torch.float16, device=dev)
+    hk = torch.empty((B, K), dtype=torch.int32, device=dev)
     out = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-    n = stack.L * steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(2 * n)]
+    names = [plan["gate_up"]] + (["moe_h_encode", plan["down"]] if shared_down else [plan["down"]])
+    times = {n: [] for n in names}
+    nbytes = {n: [] for n in names}
+    ev = []
     x = buf["x0"]
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(s):
-        i = 0
         for _ in range(steps):
             for l in range(stack.L):
                 gu, gus, dn, dns = stack.weights[l]
-                a, b = ev[i]
-                a.record(s)
-                wd.wd_moe_gate_up(x, buf["ids"][l], gu, gus, h, stream=s)
-                b.record(s)
-                a, b = ev[i + 1]
-                a.record(s)
-                wd.wd_moe_down(h, buf["ids"][l], buf["w"][l], dn, dns, out, stream=s)
-                b.record(s)
-                i += 2
+                ids, w = buf["ids"][l], buf["w"][l]
+                calls = [(names[0], lambda: wd.wd_moe_gate_up(x, ids, gu, gus, h, stream=s))]
+                if shared_down:
+                    calls.append(("moe_h_encode", lambda: wd.wd_moe_h_encode(h, h16, hk, stream=s)))
+                    calls.append((names[2], lambda: wd.wd_moe_down_encoded(h16, hk, ids, w, dn, dns,
+                                                                           out, stream=s)))
+                else:
+                    calls.append((names[1], lambda: wd.wd_moe_down(h, ids, w, dn, dns, out, stream=s)))
+                for n, fn in calls:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    fn()
+                    b.record(s)
+                    ev.append((n, l, a, b))
     torch.cuda.synchronize(dev)
-    t_gu = [ev[2 * j][0].elapsed_time(ev[2 * j][1]) for j in range(n)]
-    t_dn = [ev[2 * j + 1][0].elapsed_time(ev[2 * j + 1][1]) for j in range(n)]
-    b_gu = [gate_up_bytes(buf["ids_host"][l], B, H, I, stack.E, K) for l in range(stack.L)] * steps
-    b_dn = [down_bytes(buf["ids_host"][l], B, H, I, stack.E, K) for l in range(stack.L)] * steps
-    return dict(gate_up_ms=float(np.mean(t_gu)), down_ms=float(np.mean(t_dn)),
-                gate_up_bytes=float(np.mean(b_gu)), down_bytes=float(np.mean(b_dn)), launches=2 * n)
+    for n, l, a, b in ev:
+        times[n].append(a.elapsed_time(b))
+        ids_h = buf["ids_host"][l]
+        if n == names[0]:
+            nbytes[n].append(gate_up_bytes(ids_h, B, H, I, E, K))
+        elif n == "moe_h_encode":
+            nbytes[n].append(encode_bytes(B, I, K))
+        else:
+            nbytes[n].append(down_bytes(ids_h, B, H, I, E, K) + (4 * B * K if shared_down else 0))
+    return {n: dict(ms=float(np.mean(times[n])), bytes=float(np.mean(nbytes[n])),
+                    launches=len(times[n])) for n in names}
 
 
-def measure_copy_peak(torch, wd, dev, reps=10):
+def measure_copy_peaks(torch, wd, dev, reps=10):
+    """Best-of-reps copy bandwidth (read + write bytes) of this bench's copy
+    kernel over a few grid sizes and of torch's copy_, and the read-only
+    streaming kernel, over 2 GiB buffers."""
     n = 2 << 30
     src = torch.empty(n, dtype=torch.uint8, device=dev)
     dst = torch.empty(n, dtype=torch.uint8, device=dev)
     sink = torch.zeros(1, dtype=torch.int32, device=dev)
     wd.wd_bench_fill(src, 0x01020304)
-    best_copy = best_read = 0.0
+    sms = wd.wd_bench_sm_count()
+    best = {"copy": (0.0, 0), "read": (0.0, 0), "torch_copy": (0.0, 0)}
+
+    def timed(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b)
+
     for _ in range(reps):
-        for kind in ("copy", "read"):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            if kind == "copy":
-                wd.wd_bench_copy(dst, src)
-            else:
-                wd.wd_bench_read(src, sink)
-            b.record()
-            torch.cuda.synchronize(dev)
-            ms = a.elapsed_time(b)
-            if kind == "copy":
-                best_copy = max(best_copy, 2 * n / ms / 1e6)
-            else:
-                best_read = max(best_read, n / ms / 1e6)
+        for blocks in (4 * sms, 8 * sms, 16 * sms):
+            gbs = 2 * n / timed(lambda: wd.wd_bench_copy(dst, src, blocks=blocks)) / 1e6
+            if gbs > best["copy"][0]:
+                best["copy"] = (gbs, blocks)
+            gbs = n / timed(lambda: wd.wd_bench_read(src, sink, blocks=blocks)) / 1e6
+            if gbs > best["read"][0]:
+                best["read"] = (gbs, blocks)
+        gbs = 2 * n / timed(lambda: dst.copy_(src)) / 1e6
+        if gbs > best["torch_copy"][0]:
+            best["torch_copy"] = (gbs, 0)
     del src, dst
     spec = wd.wd_bench_spec_gbs()
-    return dict(copy_gbs=round(best_copy, 1), read_gbs=round(best_read, 1),
+    return dict(copy_gbs=round(best["copy"][0], 1), copy_blocks=best["copy"][1],
+                read_gbs=round(best["read"][0], 1), read_blocks=best["read"][1],
+                torch_copy_gbs=round(best["torch_copy"][0], 1),
                 spec_gbs=round(spec, 1) if spec > 0 else None)
 
 
@@ -344,74 +429,192 @@ def e2e_pass(torch, wd, dev, stack, buf, steps, warmup, barrier):
     return a.elapsed_time(b) / steps, h2d, out_h.numel() * 2
 
 
+def time_single_layers(torch, wd, dev, peak, iters, log):
+    """One layer of each single-layer workload, cold: before every timed call
+    the L2 is flushed by writing L2_FLUSH_BYTES (untimed); events on the
+    launching stream around the call; median over `iters` calls."""
+    rows = []
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    cases = [("qwen3_b1", (1,)), ("qwen3_sweep", SWEEP_B), ("qwen3_zipf", (32,)),
+             ("qwen3_fixed", (32,)), ("qwen3_disjoint", (32,))]
+    weights = {}
+    for name, batches in cases:
+        wl = synth.WORKLOADS[name]
+        if wl.seed not in weights:
+            weights.clear()
+            weights[wl.seed] = upload_layer(torch, dev, wl, 0)
+        gu, gus, dn, dns = weights[wl.seed]
+        for B in batches:
+            xs = synth.x(wl.seed, 0, B, wl.H)
+            ids, w = synth.route(wl.seed, 0, B, wl.E, wl.K, mode=wl.route)
+            x_d = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+            ids_d, w_d = torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev)
+            out = torch.empty((B, wl.H), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(wd.wd_moe_workspace_size(B, wl.K, wl.I), dtype=torch.uint8, device=dev)
+            wd.wd_moe_workspace_init(ws)
+            ms = []
+            with torch.cuda.stream(s):
+                for it in range(iters + 2):
+                    wd.wd_bench_fill(flush, 0x5A5A5A5A + it, stream=s)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    wd.wd_moe_decode(x_d, ids_d, w_d, gu, gus, dn, dns, out, ws, stream=s)
+                    b.record(s)
+                    torch.cuda.synchronize(dev)
+                    if it >= 2:
+                        ms.append(a.elapsed_time(b))
+            t = statistics.median(ms)
+            nb = layer_bytes(ids, B, wl.H, wl.I, wl.E, wl.K)
+            uniq = int(np.unique(ids).size)
+            plan = plan_of(wd, B, wl.H, wl.I, wl.E, wl.K)
+            rows.append({"workload": name, "B": B, "us_per_layer": round(t * 1e3, 2),
+                         "unique_experts": uniq, "unique_MB": round(nb / 1e6, 2),
+                         "GBps": round(nb / t / 1e6, 1), "frac_copy_peak": round(nb / t / 1e6 / peak, 4),
+                         "plan": f"{plan['gate_up']} + {plan['down']}"})
+            log(f"single layer {name} B={B}: {rows[-1]}")
+    del flush
+    return rows
+
+
 # ------------------------------------------------------------- CPU oracle --
 
-_SAMPLE_CACHE = {}
+def _routed_sample(l, tokens):
+    """Routing and the routed experts' weights of stack layer l for the given
+    token indices (only the routed experts are generated)."""
+    wl = WORKLOAD
+    H, I, E, K = wl.H, wl.I, wl.E, wl.K
+    ids, w = synth.route(wl.seed, l, HEADLINE_B, E, K)
+    ids, w = ids[tokens], w[tokens]
+    gu = np.zeros((E, 2 * I, H), np.uint8)
+    gus = np.zeros((E, 2 * I, H // 32), np.uint8)
+    dn = np.zeros((E, H, I), np.uint8)
+    dns = np.zeros((E, H, I // 32), np.uint8)
+    for e in np.unique(ids):
+        synth.gate_up(wl.seed, l, E, H, I, experts=(int(e), int(e) + 1), out=(gu, gus), threads=1)
+        synth.down(wl.seed, l, E, H, I, experts=(int(e), int(e) + 1), out=(dn, dns), threads=1)
+    return ids, w, gu, gus, dn, dns
 
 
-def _sample_layer(l, tokens, B):
-    """Routing and the routed experts' weights of layer l for the first `tokens`
-    tokens (untimed; only the routed experts are generated)."""
-    key = (l, tokens, B)
-    if key not in _SAMPLE_CACHE:
-        wl = WORKLOAD
-        H, I, E, K = wl.H, wl.I, wl.E, wl.K
-        ids, w = synth.route(wl.seed, l, B, E, K)
-        ids, w = ids[:tokens], w[:tokens]
-        gu = np.zeros((E, 2 * I, H), np.uint8)
-        gus = np.zeros((E, 2 * I, H // 32), np.uint8)
-        dn = np.zeros((E, H, I), np.uint8)
-        dns = np.zeros((E, H, I // 32), np.uint8)
-        for e in np.unique(ids):
-            synth.gate_up(wl.seed, l, E, H, I, experts=(int(e), int(e) + 1), out=(gu, gus))
-            synth.down(wl.seed, l, E, H, I, experts=(int(e), int(e) + 1), out=(dn, dns))
-        _SAMPLE_CACHE.clear()
-        _SAMPLE_CACHE[key] = (ids, w, gu, gus, dn, dns)
-    return _SAMPLE_CACHE[key]
-
-
-def oracle_sample(layers, tokens, B=HEADLINE_B):
-    """Time the CPU oracle (as it stands, one thread) on `tokens` tokens of the
-    stack's first `layers` layers at batch B; returns (seconds, bytes)."""
+def oracle_chain(layers, tokens, inputs=None):
+    """Run the oracle (as it stands, one thread) on the given tokens through the
+    stack's first `layers` layers; returns (seconds of oracle compute, bytes)."""
     import oracle
 
     wl = WORKLOAD
     H, I, E, K = wl.H, wl.I, wl.E, wl.K
-    xs = synth.x(wl.seed, 0, B, H)[:tokens]
+    tokens = list(tokens)
+    xs = synth.x(wl.seed, 0, HEADLINE_B, H)[tokens]
+    data = inputs if inputs is not None else [_routed_sample(l, tokens) for l in range(layers)]
     secs, nbytes = 0.0, 0
     for l in range(layers):
-        ids, w, gu, gus, dn, dns = _sample_layer(l, tokens, B)
+        ids, w, gu, gus, dn, dns = data[l]
         t0 = time.perf_counter()
         xs = oracle.moe_decode(xs, ids, w, gu, gus, dn, dns, I, E)
         secs += time.perf_counter() - t0
-        nbytes += algorithmic_bytes([ids], tokens, H, I, E, K)
+        nbytes += layer_bytes(ids, len(tokens), H, I, E, K)
     return secs, nbytes
+
+
+def _cpu_worker(layers, tokens, ready, start, results):
+    """Spawned process: generate its tokens' routed weights, signal ready,
+    then time the oracle on them once `start` is set."""
+    data = [_routed_sample(l, list(tokens)) for l in range(layers)]
+    ready.put(1)
+    start.wait()
+    secs, _ = oracle_chain(layers, tokens, inputs=data)
+    results.put(secs)
+
+
+def oracle_all_cores(layers, tokens, workers):
+    """The oracle on all host cores: `workers` spawned processes, each running
+    the unmodified single-threaded oracle on its share of the tokens (tokens
+    are independent through the stack).  Wall time from the common start to
+    the last finish; returns (seconds, bytes of the whole sample)."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
+    shares = [t for t in np.array_split(np.asarray(tokens), workers) if t.size]
+    procs = [ctx.Process(target=_cpu_worker, args=(layers, tuple(int(v) for v in t), ready, start,
+                                                   results)) for t in shares]
+    for p in procs:
+        p.start()
+    for _ in procs:
+        ready.get(timeout=600)
+    t0 = time.perf_counter()
+    start.set()
+    for _ in procs:
+        results.get(timeout=600)
+    wall = time.perf_counter() - t0
+    for p in procs:
+        p.join(timeout=60)
+    nbytes = 0
+    for l in range(layers):
+        ids, _ = synth.route(WORKLOAD.seed, l, HEADLINE_B, WORKLOAD.E, WORKLOAD.K)
+        nbytes += layer_bytes(ids[list(tokens)], len(tokens), WORKLOAD.H, WORKLOAD.I, WORKLOAD.E,
+                              WORKLOAD.K)
+    return wall, nbytes, len(procs)
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(layers=2):
+    """The oracle on a bounded sample (all 32 tokens of the stack's first
+    `layers` layers): one core, then all cores."""
+    tokens = list(range(HEADLINE_B))
+    secs1, nb = oracle_chain(layers, tokens)
+    cores = os.cpu_count() or 1
+    wall, nb_all, used = oracle_all_cores(layers, tokens, min(cores, HEADLINE_B))
+    assert nb_all == nb
+    sample = (f"layers 0..{layers - 1} of the 48-layer stack, all {HEADLINE_B} tokens, FP64 C oracle "
+              f"as it stands")
+    return {"value": round(nb / wall / 1e9, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": sample + f"; {used} processes of one thread each, {wall:.2f} s wall",
+            "single_core": {"value": round(nb / secs1 / 1e9, 4), "seconds": round(secs1, 3)},
+            "hardware_concurrency": cores, "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank):
     """The oracle as the reference arm: same metric, unit and workload; each
-    step is a bounded sample of the stack (token-layers) on one host core."""
+    step is a bounded sample of the stack (layer 0, as many of its 32 tokens as
+    the time budget allows) on all host cores."""
     if rank != 0:
         return
+    cores = os.cpu_count() or 1
     budget = float(os.environ.get("WD_REFERENCE_BUDGET_S", "150"))
-    per_tl = 0.08  # approximate seconds per token-layer of the oracle
-    tokens = max(1, min(HEADLINE_B, int(budget / (args.steps + args.warmup) / per_tl)))
+    per_tl = 0.08  # approximate seconds per token-layer of the one-thread oracle
+    tokens = max(1, min(HEADLINE_B, int(budget * cores / (args.steps + args.warmup) / per_tl)))
+    workers = min(cores, tokens)
+    sample_tokens = list(range(tokens))
     for _ in range(args.warmup):
-        oracle_sample(1, tokens)
-    secs, nbytes = 0.0, 0
+        oracle_all_cores(1, sample_tokens, workers)
+    secs, nbytes, used = 0.0, 0, 1
     for _ in range(args.steps):
-        s, b = oracle_sample(1, tokens)
+        s, b, used = oracle_all_cores(1, sample_tokens, workers)
         secs += s
         nbytes += b
     value = nbytes / secs / 1e9
-    sample = f"layer 0 of the 48-layer stack, first {tokens} of {HEADLINE_B} tokens per step"
+    sample = (f"layer 0 of the 48-layer stack, first {tokens} of {HEADLINE_B} tokens per step, "
+              f"{used} processes of the one-thread FP64 C oracle")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(HEADLINE_B),
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": sample, "hardware_concurrency": cores,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -458,6 +661,25 @@ def aggregate_gbps(local_bytes, local_ms, ranks):
     return ranks.sum(float(local_bytes)) / ranks.max(local_ms) / 1e6
 
 
+def roofline_of(kernels, hbm_peak, peaks_kind):
+    """Roofline entry of the kernel with the longest mean launch, and every
+    kernel's own figures."""
+    rows = {}
+    for n, k in kernels.items():
+        gbs = k["bytes"] / k["ms"] / 1e6
+        rows[n] = {"us_per_launch": round(k["ms"] * 1e3, 2), "algorithmic_bytes_per_launch": round(k["bytes"]),
+                   "achieved": round(gbs, 1), "frac": round(gbs / hbm_peak, 4), "launches": k["launches"]}
+    top = max(kernels, key=lambda n: kernels[n]["ms"])
+    tr = profile_traffic(top.split("<")[0], kernels[top]["bytes"])
+    r = rows[top]
+    return {"kernel": top, "bound": "hbm", "achieved": r["achieved"], "peak": hbm_peak, "unit": "GB/s",
+            "frac": r["frac"], "traffic": None if tr is None else tr["bytes_per_launch"],
+            "traffic_detail": tr, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peaks_kind})",
+            "algorithmic_bytes_per_launch": r["algorithmic_bytes_per_launch"],
+            "us_per_launch": r["us_per_launch"], "chosen_by": "longest mean launch of the plan",
+            "kernels": rows}
+
+
 # ------------------------------------------------------------------- main --
 
 def main():
@@ -471,6 +693,8 @@ def main():
     ap.add_argument("--sweep", default=",".join(map(str, SWEEP_B)))
     ap.add_argument("--sweep-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the single-layer workloads, plan comparisons and fresh-input stack")
     ap.add_argument("--quick", action="store_true", help="headline only (profiling runs)")
     args = ap.parse_args()
 
@@ -504,20 +728,31 @@ def main():
     barrier, max_over_ranks, sum_over_ranks = ranks.barrier, ranks.max, ranks.sum
 
     peaks_file, peaks_kind = read_peaks_file()
+    hbm_peak = float(peaks_file["hbm_gbs"])
     if args.quick:  # profiling runs keep the device footprint small
-        peaks = dict(copy_gbs=float(peaks_file["hbm_gbs"]), read_gbs=None, spec_gbs=None)
+        peaks = dict(copy_gbs=hbm_peak, read_gbs=None, torch_copy_gbs=None, spec_gbs=None)
     else:
-        peaks = measure_copy_peak(torch, wd, dev)
+        peaks = measure_copy_peaks(torch, wd, dev)
         torch.cuda.empty_cache()
-    log(f"copy peak {peaks['copy_gbs']} GB/s, read peak {peaks['read_gbs']} GB/s")
+    # the fractions are taken against the largest copy bandwidth measured on this GPU
+    peak_ref = max(v for v in (peaks["copy_gbs"], peaks.get("torch_copy_gbs"), hbm_peak) if v)
+    log(f"peaks {peaks}, fraction denominator {peak_ref} GB/s")
 
     sweep = [int(b) for b in args.sweep.split(",") if b] if not args.quick else []
     max_b = max([HEADLINE_B] + sweep)
     stack = Stack(torch, wd, dev, args.layers, max_b, log)
     H, I, E, K = stack.H, stack.I, stack.E, stack.K
 
+    def stack_row(B, ms, nb, plan_name=None):
+        plan = plan_of(wd, B, H, I, E, K)
+        return {"B": B, "us_per_layer": round(ms * 1e3 / stack.L, 2), "GBps": round(nb / ms / 1e6, 1),
+                "frac_copy_peak": round(nb / ms / 1e6 / peak_ref, 4),
+                "unique_MB_per_layer": round(nb / stack.L / 1e6, 2),
+                "plan": plan_name or "built-in",
+                "kernels": f"{plan['gate_up']} + {plan['down']} (pdl={plan['pdl']})"}
+
     # ---- sweep over B (each B: its own routing and graph) ----
-    sweep_rows = []
+    sweep_rows, compare_rows = [], []
     for B in sweep:
         if B == HEADLINE_B:
             continue
@@ -525,10 +760,7 @@ def main():
         g, s = stack.graph(buf)
         ms = max_over_ranks(time_graph(torch, dev, g, s, args.sweep_steps, 3, barrier))
         nb = algorithmic_bytes(buf["ids_host"], B, H, I, E, K)
-        sweep_rows.append({"B": B, "us_per_layer": round(ms * 1e3 / stack.L, 2),
-                           "GBps": round(nb / ms / 1e6, 1),
-                           "frac_copy_peak": round(nb / ms / 1e6 / peaks["copy_gbs"], 4),
-                           "unique_MB_per_layer": round(nb / stack.L / 1e6, 2)})
+        sweep_rows.append(stack_row(B, ms, nb))
         del g
         log(f"B={B}: {sweep_rows[-1]}")
 
@@ -543,32 +775,44 @@ def main():
     total_bytes = sum_over_ranks(float(nb))
     value = aggregate_gbps(nb, ms_local, ranks)  # all ranks' bytes / the slowest rank's time
     per_rank_gbs = nb / ms / 1e6
-    sweep_rows.append({"B": B, "us_per_layer": round(ms * 1e3 / stack.L, 2),
-                       "GBps": round(per_rank_gbs, 1),
-                       "frac_copy_peak": round(per_rank_gbs / peaks["copy_gbs"], 4),
-                       "unique_MB_per_layer": round(nb / stack.L / 1e6, 2)})
+    sweep_rows.append(stack_row(B, ms, nb))
     sweep_rows.sort(key=lambda r: r["B"])
     log(f"B=32 headline: {ms:.3f} ms/step, {per_rank_gbs:.1f} GB/s per GPU")
+    del g
 
-    # ---- roofline of the dominant kernel (each kernel timed alone, cold) ----
+    # ---- roofline of the kernel with the longest launch (each kernel timed alone, cold) ----
     kt = time_kernels_alone(torch, wd, dev, stack, buf, steps=max(2, min(10, args.steps // 20)))
-    gu_gbs = kt["gate_up_bytes"] / kt["gate_up_ms"] / 1e6
-    dn_gbs = kt["down_bytes"] / kt["down_ms"] / 1e6
-    hbm_peak = float(peaks_file["hbm_gbs"])
-    # the kernels the plan launches at this shape, e.g. "gate_up=moe_gate_up_persist<2,1> down=..."
-    plan = dict(kv.split("=", 1) for kv in wd.wd_moe_describe_plan(B, H, I, E, K).split())
-    gu_name, dn_name = plan["gate_up"], plan["down"]
-    traffic = profile_traffic(gu_name.split("<")[0])
-    roofline = {"kernel": gu_name, "bound": "hbm", "achieved": round(gu_gbs, 1),
-                "peak": hbm_peak, "unit": "GB/s", "frac": round(gu_gbs / hbm_peak, 4),
-                "traffic": traffic, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peaks_kind})",
-                "algorithmic_bytes_per_launch": round(kt["gate_up_bytes"]),
-                "us_per_launch": round(kt["gate_up_ms"] * 1e3, 2),
-                "second_kernel": {"kernel": dn_name, "achieved": round(dn_gbs, 1),
-                                  "frac": round(dn_gbs / hbm_peak, 4),
-                                  "algorithmic_bytes_per_launch": round(kt["down_bytes"]),
-                                  "us_per_launch": round(kt["down_ms"] * 1e3, 2),
-                                  "traffic": profile_traffic(dn_name.split("<")[0])}}
+    roofline = roofline_of(kt, hbm_peak, peaks_kind)
+    log(f"roofline {roofline['kernel']}: {roofline['achieved']} GB/s = {roofline['frac']} of measured")
+
+    extras = {}
+    if not args.quick and not args.no_extras:
+        # ---- other plans on the same stack, B = 8..32 ----
+        for name, spec in COMPARE_PLANS.items():
+            wd.wd_moe_set_plan(spec)
+            try:
+                for Bc in [b for b in (8, 16, 32) if b in sweep + [HEADLINE_B]]:
+                    bc = stack.buffers(Bc)
+                    g, s = stack.graph(bc)
+                    msc = max_over_ranks(time_graph(torch, dev, g, s, args.sweep_steps, 3, barrier))
+                    compare_rows.append(stack_row(Bc, msc, algorithmic_bytes(bc["ids_host"], Bc, H, I, E, K),
+                                                  plan_name=f"{name}: {spec}"))
+                    del g
+                    log(f"plan {name} B={Bc}: {compare_rows[-1]}")
+            finally:
+                wd.wd_moe_set_plan(None)
+        # ---- the stack with fresh activations at every layer (timing only) ----
+        fresh = []
+        for Bf in (1, HEADLINE_B):
+            bf = stack.buffers(Bf, fresh_inputs=True)
+            g, s = stack.graph(bf)
+            msf = max_over_ranks(time_graph(torch, dev, g, s, args.sweep_steps, 3, barrier))
+            fresh.append(stack_row(Bf, msf, algorithmic_bytes(bf["ids_host"], Bf, H, I, E, K)))
+            del g
+        extras["fresh_inputs_stack"] = {
+            "what": "every layer reads its own seeded N(0,1) activations instead of the previous "
+                    "layer's output, so no layer runs on zeros (timing only)", "rows": fresh}
+        log(f"fresh-input stack: {fresh}")
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -582,23 +826,33 @@ def main():
                "how": "pinned H2D of x and all layers' ids/w, one wd_moe_decode call per layer "
                       "(no graph), D2H of out, events on the launching stream"}
 
+    if not args.quick and not args.no_extras:
+        del stack
+        torch.cuda.empty_cache()
+        extras["single_layers_cold"] = {
+            "what": "one layer of each single-layer workload, L2 flushed (512 MB written) before "
+                    "every timed call, median of 20 calls",
+            "rows": time_single_layers(torch, wd, dev, peak_ref, 20, log)}
+
     # ---- CPU oracle on a bounded sample (rank 0) ----
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and not args.quick:
-        secs, sb = oracle_sample(layers=1, tokens=B)
-        cpu = {"value": round(sb / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"layer 0 of the stack, all {B} tokens ({secs:.1f} s, FP64 C, one thread)"}
+        cpu = cpu_baseline(layers=2)
+        log(f"cpu baseline {cpu}")
 
-    launches = args.steps * stack.L * wd.wd_moe_launches_per_call()
+    launches = args.steps * stack_launches(wd, args.layers, B, H, I, E, K)
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded Philox; Qwen-3-style shapes, random-init MXFP8 weights)",
             "config": config_dict(B),
-            "us_per_layer": round(ms * 1e3 / stack.L, 3),
-            "frac_copy_peak": round(per_rank_gbs / peaks["copy_gbs"], 4),
+            "us_per_layer": round(ms * 1e3 / args.layers, 3),
+            "frac_copy_peak": round(per_rank_gbs / peak_ref, 4),
+            "frac_copy_peak_denominator": {"gbs": peak_ref,
+                                           "is": "max(own copy kernel, torch copy_, MEASURED_PEAKS hbm_gbs)"},
             "peaks": {**peaks, "measured_peaks_json_hbm_gbs": hbm_peak},
-            "sweep": sweep_rows, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "sweep": sweep_rows, "plan_comparison": compare_rows, **extras,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
             "context": {"pages_b200": "3.95 TB/s at B=32 = 58% of a 6.8 TB/s copy peak (B200)"}}
     if args.quick or args.layers != WORKLOAD.layers:
@@ -607,6 +861,11 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def stack_launches(wd, layers, B, H, I, E, K):
+    """Kernel launches of one step of the stack under the built-in plan."""
+    return layers * wd.wd_moe_launches(B, H, I, E, K)
 
 
 if __name__ == "__main__":

@@ -5,14 +5,16 @@
  * section 硬件效率 [Hardware efficiency]) states its layer throughput as a
  * fraction of the peak a copy kernel reaches with sequential reads.  These
  * kernels give that denominator on the machine at hand:
- *   wd_bench_copy  - dst[i] = src[i], 32-byte vectors, grid-stride; bytes moved
- *                    = 2 * bytes (read + write), the copy-kernel convention;
+ *   wd_bench_copy  - dst[i] = src[i], 32-byte vectors, grid-stride with four
+ *                    loads in flight per thread; bytes moved = 2 * bytes
+ *                    (read + write), the copy-kernel convention;
  *   wd_bench_read  - streams src once (read only) and folds it into *sink;
  *   wd_bench_fill  - writes a pattern over buf (used to evict L2 between timed
  *                    runs when buf is larger than L2).
  * All pointers are device pointers owned by the caller; src/dst/buf must be
- * 32-byte aligned and `bytes` a multiple of 32.  Asynchronous on `stream`;
- * returns 0 on success, else the cudaError_t of the launch.
+ * 32-byte aligned and `bytes` a multiple of 32.  `blocks` is the grid size
+ * (0: 8 CTAs of 256 threads per SM).  Asynchronous on `stream`; returns 0 on
+ * success, else the cudaError_t of the launch.
  */
 #ifndef WD_BENCH_H_
 #define WD_BENCH_H_

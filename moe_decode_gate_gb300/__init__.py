@@ -1,18 +1,22 @@
 """GB300-native small-batch MoE decode layer on MXFP8 weights ("warp decode").
 
-Two hand-written sm_103a CUDA kernels behind a C-ABI (include/wd_moe.h):
+Hand-written sm_103a CUDA kernels behind a C-ABI (include/wd_moe.h).  While
+tokens rarely share experts (2*B*K < E) the layer is the pages' two kernels:
 ``moe_gate_up_3d_batched`` (one warp per token x routed expert x neuron group)
 and ``moe_down_3d_batched`` (one warp per token x output-dim group, all K
-experts folded into one FP32 register accumulator); for batches whose tokens
-share experts the gate/up stage runs ``moe_gate_up_persist``, which reads and
-dequantises each routed expert row once for all of its tokens
-(``wd_moe_describe_plan`` names the kernels a shape gets).  This package is the
-thin Python binding over that library; PyTorch only supplies device memory and
-streams.
+experts folded into one FP32 register accumulator).  Once they share experts
+each routed row is read and dequantised once for all of its tokens:
+``moe_gate_up_mma`` (tensor-core products, one CTA per SM), then
+``moe_h_encode`` and ``moe_down_dimblock`` (one CTA per 16 output dims over
+every routed expert); ``wd_moe_describe_plan`` names the kernels a shape gets.
+This package is the thin Python binding over that library; PyTorch only
+supplies device memory and streams.
 
     from moe_decode_gate_gb300 import wd_moe_decode, wd_moe_workspace_size
 """
 from ._native import (  # noqa: F401
+    FLAG_BAD_EXPERT_ID,
+    FLAG_PIPELINE_TIMEOUT,
     SIGNATURES,
     WdError,
     library_path,
@@ -27,6 +31,10 @@ from ._native import (  # noqa: F401
     wd_moe_describe_plan,
     wd_last_error_string,
     wd_moe_down,
+    wd_moe_down_encoded,
+    wd_moe_down_workspace,
+    wd_moe_h_encode,
+    wd_moe_launches,
     wd_moe_gate_up,
     wd_moe_launches_per_call,
     wd_moe_read_error_flag,

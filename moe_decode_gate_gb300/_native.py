@@ -19,7 +19,11 @@ _LIB = None
 
 WD_OK = 0
 STATUS_NAMES = {0: "WD_OK", 1: "WD_ERR_INVALID_ARG", 2: "WD_ERR_UNSUPPORTED_SHAPE",
-                3: "WD_ERR_WORKSPACE_TOO_SMALL", 4: "WD_ERR_CUDA", 5: "WD_ERR_BAD_EXPERT_ID"}
+                3: "WD_ERR_WORKSPACE_TOO_SMALL", 4: "WD_ERR_CUDA", 5: "WD_ERR_BAD_EXPERT_ID",
+                6: "WD_ERR_PIPELINE_TIMEOUT"}
+# bits of the workspace error flag (wd_moe_read_error_flag)
+FLAG_BAD_EXPERT_ID = 1
+FLAG_PIPELINE_TIMEOUT = 2
 
 # (name, restype, argtypes) for every symbol the headers declare
 _P, _I, _SZ, _U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
@@ -30,6 +34,10 @@ SIGNATURES = {
     "wd_moe_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _P]),
     "wd_moe_gate_up": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_moe_down": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_down_workspace": (_I, [_P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _P]),
+    "wd_moe_launches": (_I, [_I, _I, _I, _I, _I]),
+    "wd_moe_h_encode": (_I, [_P, _P, _P, _I, _I, _P]),
+    "wd_moe_down_encoded": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wd_moe_read_error_flag": (_I, [_P, _SZ, _P, ctypes.POINTER(_I)]),
     "wd_moe_launches_per_call": (_I, []),
     "wd_moe_decode_no_alloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -151,18 +159,60 @@ def wd_moe_down(h, topk_ids, topk_w, down, down_scale, out, error_flag=None, str
         _ptr(error_flag), B, H, I, E, K, _stream(stream)))
 
 
-def wd_moe_read_error_flag(workspace, stream=None) -> int:
-    """1 if an expert id was out of range since the last read (synchronises)."""
+def wd_moe_down_workspace(h, topk_ids, topk_w, down, down_scale, out, workspace, stream=None):
+    """out[B,H] (bf16) from the down stage alone with a workspace (the plan's
+    down kernels, as wd_moe_decode runs them), given h[B,K,I]."""
+    B, K, I = h.shape
+    E, H, I2 = down.shape
+    if I2 != I or topk_ids.shape != (B, K):
+        raise ValueError("inconsistent shapes")
+    _check("wd_moe_down_workspace", lib().wd_moe_down_workspace(
+        _ptr(h), _ptr(topk_ids), _ptr(topk_w), _ptr(down), _ptr(down_scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, I, E, K,
+        _stream(stream)))
+
+
+def wd_moe_h_encode(h, h16, hk, stream=None):
+    """h16 (fp16, h's shape) and hk (int32 per row) from h [..., I] (bf16)."""
+    I = h.shape[-1]
+    rows = h.numel() // I
+    _check("wd_moe_h_encode", lib().wd_moe_h_encode(_ptr(h), _ptr(h16), _ptr(hk), rows, I,
+                                                    _stream(stream)))
+
+
+def wd_moe_down_encoded(h16, hk, topk_ids, topk_w, down, down_scale, out, error_flag=None,
+                        stream=None):
+    """out[B,H] (bf16) from moe_down_dimblock alone, given moe_h_encode's output."""
+    B, K, I = h16.shape
+    E, H, I2 = down.shape
+    if I2 != I or topk_ids.shape != (B, K):
+        raise ValueError("inconsistent shapes")
+    _check("wd_moe_down_encoded", lib().wd_moe_down_encoded(
+        _ptr(h16), _ptr(hk), _ptr(topk_ids), _ptr(topk_w), _ptr(down), _ptr(down_scale), _ptr(out),
+        _ptr(error_flag), B, H, I, E, K, _stream(stream)))
+
+
+def wd_moe_read_error_flag(workspace, stream=None, with_status=False):
+    """The error-flag bit mask accumulated since the last read, then cleared
+    (synchronises): bit 0 (FLAG_BAD_EXPERT_ID) an out-of-range expert id was
+    skipped; bit 1 (FLAG_PIPELINE_TIMEOUT) a kernel's bounded wait ran out and
+    that call's output is invalid.  With ``with_status`` also the C status."""
     flag = ctypes.c_int(0)
     st = lib().wd_moe_read_error_flag(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(stream), ctypes.byref(flag))
-    if st not in (WD_OK, 5):
+    if st not in (WD_OK, 5, 6):
         raise WdError("wd_moe_read_error_flag", st)
-    return flag.value
+    return (flag.value, st) if with_status else flag.value
 
 
 def wd_moe_launches_per_call() -> int:
+    """The most kernel launches one wd_moe_decode call issues."""
     return int(lib().wd_moe_launches_per_call())
+
+
+def wd_moe_launches(B, H, I, E, K) -> int:
+    """Kernel launches wd_moe_decode issues for this shape under the current plan."""
+    return int(lib().wd_moe_launches(B, H, I, E, K))
 
 
 def wd_moe_set_plan(spec=None):
@@ -186,7 +236,8 @@ def wd_moe_describe_plan(B, H, I, E, K) -> str:
 def wd_moe_decode_no_alloc(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out,
                            stream=None):
     """The layer without a workspace, for callers that cannot allocate device
-    memory: h lives in a 1 MiB array inside the library (B*K*I*2 <= 1 MiB).
+    memory: its scratch lives in a 2 MiB array inside the library
+    (wd_moe_workspace_size(B, K, I) <= 2 MiB, i.e. B <= 85 at K=8, I=768).
     Calls that may overlap on the GPU share that array and must not be issued."""
     B, H, I, E, K = _dims(x, topk_ids, gate_up)
     _check("wd_moe_decode_no_alloc", lib().wd_moe_decode_no_alloc(

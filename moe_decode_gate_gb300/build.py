@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libwd_moe.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["wd_gate_up.cu", "wd_gate_up_rowshare.cu", "wd_gate_up_stream.cu", "wd_gate_up_mixed.cu", "wd_gate_up_persist.cu", "wd_gate_up_ring.cu", "wd_gate_up_tma.cu", "wd_gate_up_mma.cu", "wd_down.cu", "wd_down_stream.cu", "wd_down_shared.cu", "wd_down_mma.cu", "wd_down_wmma.cu", "wd_down_expert_mma.cu", "wd_capi.cu", "wd_bench.cu", "wd_no_alloc.cu"]
+SOURCES = ["wd_gate_up.cu", "wd_gate_up_rowshare.cu", "wd_gate_up_persist.cu", "wd_gate_up_mma.cu",
+           "wd_down.cu", "wd_down_dimblock.cu", "wd_capi.cu", "wd_bench.cu", "wd_no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-Xcompiler", "-Wall", "-I", os.path.join(ROOT, "include")]

@@ -8,8 +8,25 @@
 
 namespace {
 
-// 32 bytes, read-only, no L1 allocation; volatile, so each load is issued
-// exactly where it is written (the peaks stay what these loops measure).
+// 32 bytes, read-only, no L1 allocation.  The copy kernel's loads are plain
+// asm (the compiler may batch them: their values feed the stores); the read
+// kernel's are volatile so that its loop is issued as written.
+__device__ __forceinline__ wd::U32x8 ld_copy_32B(const void* p) {
+  wd::U32x8 r;
+  asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]), "=r"(r.v[5]),
+        "=r"(r.v[6]), "=r"(r.v[7])
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_32B(void* p, const wd::U32x8& v) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.v[0]),
+               "r"(v.v[1]), "r"(v.v[2]), "r"(v.v[3]), "r"(v.v[4]), "r"(v.v[5]), "r"(v.v[6]),
+               "r"(v.v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ wd::U32x8 ld_stream_32B(const void* p) {
   wd::U32x8 r;
   asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -19,16 +36,23 @@ __device__ __forceinline__ wd::U32x8 ld_stream_32B(const void* p) {
   return r;
 }
 
+// Grid-stride copy with four 32-byte loads in flight per thread before their
+// stores.
 __global__ void __launch_bounds__(256) copy_kernel(uint8_t* __restrict__ dst,
                                                    const uint8_t* __restrict__ src, size_t n32) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += stride) {
-    const wd::U32x8 v = ld_stream_32B(src + i * 32);
-    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + i * 32),
-                 "r"(v.v[0]), "r"(v.v[1]), "r"(v.v[2]), "r"(v.v[3]), "r"(v.v[4]), "r"(v.v[5]),
-                 "r"(v.v[6]), "r"(v.v[7])
-                 : "memory");
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n32; i += 4 * stride) {
+    const wd::U32x8 a = ld_copy_32B(src + i * 32);
+    const wd::U32x8 b = ld_copy_32B(src + (i + stride) * 32);
+    const wd::U32x8 c = ld_copy_32B(src + (i + 2 * stride) * 32);
+    const wd::U32x8 d = ld_copy_32B(src + (i + 3 * stride) * 32);
+    st_32B(dst + i * 32, a);
+    st_32B(dst + (i + stride) * 32, b);
+    st_32B(dst + (i + 2 * stride) * 32, c);
+    st_32B(dst + (i + 3 * stride) * 32, d);
   }
+  for (; i < n32; i += stride) st_32B(dst + i * 32, ld_copy_32B(src + i * 32));
 }
 
 __global__ void __launch_bounds__(256) read_kernel(const uint8_t* __restrict__ src, size_t n32,

@@ -21,14 +21,8 @@
 //     down rows stream in while the gate/up kernel finishes;
 //   - warps are numbered output-dim-major, token-minor, so tokens that share
 //     an expert read its rows while they are still in L2.
-//
-// The persistent form (moe_down_3d_batched_persist) runs one wave of CTAs
-// whose warps walk the same (token, output-dim group) items with a stride of
-// all warps of the grid; lanes 0..K-1 ask L2 (cp.async.bulk.prefetch) for the
-// next item's K routed row groups while the warp computes the current one.
 #include "wd_device.cuh"
 #include "wd_launch.h"
-#include "wd_pipeline.cuh"
 
 namespace wd {
 
@@ -115,150 +109,6 @@ __global__ void __launch_bounds__(256, 2) moe_down_3d_batched(
   if (error_flag && __any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(error_flag, 1u);
 }
 
-// One (token b, output dims d0..d0+RPW-1) item of the down projection: the
-// loop body of moe_down_3d_batched, returning the RPW reduced outputs in
-// every lane.
-template <int RPW, int QPL>
-__device__ __forceinline__ void down_item(const uint8_t* __restrict__ hb,
-                                          const int32_t* __restrict__ ids,
-                                          const float* __restrict__ tw,
-                                          const uint8_t* __restrict__ down,
-                                          const uint8_t* __restrict__ down_scale, int H, int I,
-                                          int E, int K, int d0, unsigned long long ib_magic,
-                                          float (&y)[RPW], bool& bad) {
-  const int lane = threadIdx.x & 31;
-  const int ib = I >> 5;
-  const int nq = K * ib;
-  float acc[RPW];
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) acc[r] = 0.0f;
-  for (int q0 = 0; q0 < nq; q0 += 32 * QPL) {
-    U32x8 wd[RPW][QPL];
-    uint32_t sd[RPW][QPL];
-    float wk[QPL];
-    int hoff[QPL];
-    bool ok[QPL];
-#pragma unroll
-    for (int j = 0; j < QPL; ++j) {
-      const int q = q0 + lane + 32 * j;
-      ok[j] = false;
-      if (q < nq) {
-        const int k = (int)(((unsigned long long)q * ib_magic) >> 32);
-        const int blk = q - k * ib;
-        const int e = __ldg(ids + k);
-        if (e >= 0 && e < E) {
-          ok[j] = true;
-          wk[j] = __ldg(tw + k);
-          hoff[j] = (k * I + blk * 32) * 2;
-          const size_t row0 = (size_t)e * H + d0;
-#pragma unroll
-          for (int r = 0; r < RPW; ++r) {
-            wd[r][j] = ld_weights_32B(down + (row0 + r) * I + (size_t)blk * 32);
-            sd[r][j] = ld_scale(down_scale + (row0 + r) * ib + blk);
-          }
-        } else {
-          bad = true;
-        }
-      }
-    }
-    // h comes from the first kernel (the wait returns at once after the first)
-    const uint32_t wait_token = grid_dependency_wait();
-#pragma unroll
-    for (int j = 0; j < QPL; ++j) {
-      if (ok[j]) {
-        const U32x8 ha = ld_act_32B(hb + hoff[j] + wait_token);
-        const U32x8 hc = ld_act_32B(hb + hoff[j] + wait_token + 32);
-        float2 hf[16];
-        unpack_act32(ha, hc, hf);
-#pragma unroll
-        for (int r = 0; r < RPW; ++r)
-          acc[r] = fmaf(wk[j] * e8m0_to_f32(sd[r][j]), block_dot(wd[r][j], hf), acc[r]);
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < RPW; ++r) y[r] = warp_sum(acc[r]);
-}
-
-template <int RPW, int QPL>
-__global__ void __launch_bounds__(256, 2) moe_down_3d_batched_persist(
-    const __nv_bfloat16* __restrict__ h, const int32_t* __restrict__ topk_ids,
-    const float* __restrict__ topk_w, const uint8_t* __restrict__ down,
-    const uint8_t* __restrict__ down_scale, __nv_bfloat16* __restrict__ out,
-    uint32_t* __restrict__ error_flag, int B, int H, int I, int E, int K,
-    unsigned long long ib_magic) {
-  grid_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long total = (long long)(H / RPW) * B;
-  const int ib = I >> 5;
-  bool bad = false;
-
-  // lanes k < K: the item's k-th routed row group (RPW rows of I codes + scales)
-  auto prefetch_item = [&](long long gw) {
-    if (gw >= total) return;
-    const int grp = (int)(gw / B);
-    const int b = (int)(gw - (long long)grp * B);
-    for (int k = lane; k < K; k += 32) {
-      const int e = __ldg(topk_ids + (size_t)b * K + k);
-      if (e >= 0 && e < E) {
-        const size_t row0 = (size_t)e * H + (size_t)grp * RPW;
-        prefetch_l2_bulk(down + row0 * I, (uint32_t)(RPW * I));
-        prefetch_l2_bulk(down_scale + row0 * ib, (uint32_t)(RPW * ib));
-      }
-    }
-  };
-
-  long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  prefetch_item(gw);
-  for (; gw < total; gw += nwarps) {
-    prefetch_item(gw + nwarps);
-    const int grp = (int)(gw / B);
-    const int b = (int)(gw - (long long)grp * B);
-    const int d0 = grp * RPW;
-    float y[RPW];
-    down_item<RPW, QPL>(reinterpret_cast<const uint8_t*>(h + (size_t)b * K * I),
-                        topk_ids + (size_t)b * K, topk_w + (size_t)b * K, down, down_scale, H, I,
-                        E, K, d0, ib_magic, y, bad);
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-      if (lane == r) out[(size_t)b * H + d0 + r] = __float2bfloat16_rn(y[r]);
-  }
-  if (error_flag && __any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(error_flag, 1u);
-}
-
-template <int RPW, int QPL>
-static cudaError_t launch_down_persist_t(const DownArgs& a, cudaStream_t stream, bool pdl) {
-  static int ctas_per_sm = 0;
-  if (ctas_per_sm == 0) {
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &ctas_per_sm, moe_down_3d_batched_persist<RPW, QPL>, 256, 0);
-    if (e != cudaSuccess) return e;
-    if (ctas_per_sm < 1) ctas_per_sm = 1;
-  }
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long warps = (long long)(a.H / RPW) * a.B;
-  const long long need = (warps + 7) / 8;
-  const long long grid = need < (long long)ctas_per_sm * sms ? need : (long long)ctas_per_sm * sms;
-  const unsigned long long ib = (unsigned long long)(a.I / 32);
-  const unsigned long long ib_magic = ((1ull << 32) + ib - 1) / ib;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_down_3d_batched_persist<RPW, QPL>,
-                            reinterpret_cast<const __nv_bfloat16*>(a.h), a.topk_ids, a.topk_w,
-                            a.down, a.down_scale, reinterpret_cast<__nv_bfloat16*>(a.out),
-                            a.error_flag, a.B, a.H, a.I, a.E, a.K, ib_magic);
-}
-
 template <int RPW, int QPL>
 static cudaError_t launch_down_t(const DownArgs& a, cudaStream_t stream, bool pdl) {
   const long long warps = (long long)(a.H / RPW) * a.B;
@@ -281,18 +131,6 @@ static cudaError_t launch_down_t(const DownArgs& a, cudaStream_t stream, bool pd
 }
 
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl) {
-  if (p.variant == kDownStream) return launch_down_stream(a, p, stream, pdl);
-  if (p.variant == kDownShared) return launch_down_shared(a, p, stream, pdl);
-  if (p.variant == kDownMma) return launch_down_mma(a, p, stream, pdl);
-  if (p.variant == kDown3dMma) return launch_down_3d_mma(a, p, stream, pdl);
-  if (p.variant == kDownExpertMma) return launch_down_expert_mma(a, p, stream, pdl);
-  if (p.variant == kDownPersist) {
-    if (p.rpw == 4 && p.qpl == 1) return launch_down_persist_t<4, 1>(a, stream, pdl);
-    if (p.rpw == 2 && p.qpl == 1) return launch_down_persist_t<2, 1>(a, stream, pdl);
-    if (p.rpw == 2 && p.qpl == 3) return launch_down_persist_t<2, 3>(a, stream, pdl);
-    if (p.rpw == 1 && p.qpl == 6) return launch_down_persist_t<1, 6>(a, stream, pdl);
-    return cudaErrorInvalidConfiguration;
-  }
 #define WD_DN_CASE(RPW, QPL) \
   if (p.rpw == RPW && p.qpl == QPL) return launch_down_t<RPW, QPL>(a, stream, pdl);
   WD_DN_CASE(1, 1)

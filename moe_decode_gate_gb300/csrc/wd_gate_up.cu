@@ -130,11 +130,7 @@ static cudaError_t launch_gate_up_t(const GateUpArgs& a, cudaStream_t stream, bo
 cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                            bool pdl) {
   if (p.variant == kGateUpRowShare) return launch_gate_up_rowshare(a, p, stream, pdl);
-  if (p.variant == kGateUpStream) return launch_gate_up_stream(a, p, stream, pdl);
-  if (p.variant == kGateUpMixed) return launch_gate_up_mixed(a, p, stream, pdl);
   if (p.variant == kGateUpPersist) return launch_gate_up_persist(a, p, stream, pdl);
-  if (p.variant == kGateUpRing) return launch_gate_up_ring(a, p, stream, pdl);
-  if (p.variant == kGateUpTma) return launch_gate_up_tma(a, p, stream, pdl);
   if (p.variant == kGateUpMma) return launch_gate_up_mma(a, p, stream, pdl);
 #define WD_GU_CASE(NPW, CPL) \
   if (p.npw == NPW && p.cpl == CPL) return launch_gate_up_t<NPW, CPL>(a, stream, pdl);

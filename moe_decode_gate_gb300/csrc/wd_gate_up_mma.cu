@@ -496,12 +496,10 @@ bool gate_up_mma_supported(int B, int H, int I, int E, int K) {
 template <int NW>
 static cudaError_t launch_mma_t(const GateUpArgs& a, int S, cudaStream_t stream, bool pdl) {
   const int smem = mma_layout(a.H, S).total;
-  static int configured = 0;
-  if (configured < smem) {
-    const cudaError_t e = cudaFuncSetAttribute(moe_gate_up_mma<NW>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  {
+    const cudaError_t e =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(moe_gate_up_mma<NW>), smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   CUtensorMap map, smap;
   if (!encode_row_slab_map(&map, a.gate_up, (uint64_t)a.E * 2 * a.I, a.H) ||

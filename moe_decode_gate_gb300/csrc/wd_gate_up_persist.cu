@@ -208,12 +208,10 @@ bool gate_up_persist_supported(int B, int H, int I, int E, int K) {
 template <int NPW, int MINB, int PFD>
 static cudaError_t launch_persist_t(const GateUpArgs& a, cudaStream_t stream, bool pdl) {
   const int smem = persist_smem_bytes(a.H);
-  static int configured = 0;
-  if (configured < smem) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        moe_gate_up_persist<NPW, MINB, PFD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  {
+    const cudaError_t e = ensure_dynamic_smem(
+        reinterpret_cast<const void*>(moe_gate_up_persist<NPW, MINB, PFD>), smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
   }
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/wd_moe.h"
+
 namespace wd {
 
 struct GateUpArgs {
@@ -30,18 +32,14 @@ struct DownArgs {
 // Limits of the shared-row gate/up variant (shared-memory routing tables).
 constexpr int kRowShareMaxSlots = 2048;    // B * K
 constexpr int kRowShareMaxExperts = 4096;  // E
-// Limit of the streamed variants' per-CTA routing tables (B * K).
+// Limit of the per-CTA routing tables of the persistent kernels (B * K).
 constexpr int kStreamMaxSlots = 256;
 
 enum GateUpVariant {
   kGateUpBatched = 0,   // moe_gate_up_3d_batched: one warp per (token, slot, neuron group)
   kGateUpRowShare = 1,  // moe_gate_up_rowshare: one warp per (expert, neuron group), all its tokens
-  kGateUpStream = 2,    // moe_gate_up_stream: rows streamed by bulk copies through shared memory
-  kGateUpMixed = 3,     // moe_gate_up_mixed: streamed rows, FP16 x FP16 -> FP32 products
-  kGateUpPersist = 4,   // moe_gate_up_persist: one wave of CTAs over shared expert rows, x staged
-  kGateUpRing = 5,      // moe_gate_up_ring: as persist, rows through a per-warp bulk-copy ring
-  kGateUpTma = 6,       // moe_gate_up_tma: as persist, rows by 2-D TMA into a CTA-wide ring
-  kGateUpMma = 7,       // moe_gate_up_mma: as persist, products by warp-level tensor-core MMAs
+  kGateUpPersist = 2,   // moe_gate_up_persist: one wave of CTAs over shared expert rows, x staged
+  kGateUpMma = 3,       // moe_gate_up_mma: as persist, products by warp-level tensor-core MMAs
 };
 
 // Compile-time shape of one kernel instance.
@@ -52,61 +50,64 @@ struct GateUpPlan {
                 // rowshare, persist: words (4 elements) dequantised per step, 1 or 2
 };
 enum DownVariant {
-  kDownBatched = 0,  // moe_down_3d_batched: one warp per (token, output-dim group)
-  kDownStream = 1,   // moe_down_stream: rows streamed by bulk copies, lane = token accumulator
-  kDownPersist = 2,  // moe_down_3d_batched_persist: batched items walked by one wave of CTAs
-  kDownShared = 3,   // moe_down_shared: CTA per output-dim group, expert rows shared by tokens
-  kDownMma = 4,      // moe_down_mma: CTA per 16 output dims, products by tensor-core MMAs
-  kDown3dMma = 5,    // moe_down_3d_mma: as batched, warp = (token, 16 dims), dots by MMAs
-  kDownExpertMma = 6,  // moe_down_expert_mma: CTA per 16 output dims, warp per routed-expert step
+  kDownBatched = 0,   // moe_down_3d_batched: one warp per (token, output-dim group)
+  kDownDimBlock = 1,  // moe_h_encode + moe_down_dimblock: CTA per 16 output dims, all experts
 };
 struct DownPlan {
-  int rpw;          // batched, persist: output dims per warp
-  int qpl;          // batched, persist: virtual blocks per lane per pass; stream: ring stages
+  int rpw;          // batched: output dims per warp; dimblock: consumer warps
+  int qpl;          // batched: virtual blocks per lane per pass; dimblock: ring stages
   int variant = 0;  // DownVariant
+  int pairs = 0;    // dimblock: (token, slot) pairs per step
 };
 
 GateUpPlan plan_gate_up(int B, int H, int I, int K, int E);
 DownPlan plan_down(int B, int H, int I, int K, int E);
+DownPlan batched_down_plan(int B, int I, int K);
 // The plans above, downgraded to a non-streamed kernel when the bulk copies'
 // 16-byte alignment does not hold for the given pointers.
 GateUpPlan plan_gate_up_for(const GateUpArgs& a);
-int pdl_mask_for(const GateUpPlan& g);
+int pdl_mask_for(const GateUpPlan& g, const DownPlan& d);
+int launches_for(const DownPlan& d);
 DownPlan plan_down_for(const DownArgs& a);
+
+// Scratch of one layer call: [0, 256) error flag, h BF16 [B,K,I], h FP16
+// [B,K,I], per-row exponents int32 [B,K] (regions rounded to 256 bytes).
+size_t layer_scratch_h_bytes(int B, int K, int I);
+size_t layer_scratch_bytes(int B, int K, int I);
+// The down stage of a call (pdl bit 0: its first launch, bit 1: its second).
+cudaError_t launch_down_stage(const DownArgs& a, const DownPlan& p, void* h16, int32_t* hk,
+                              cudaStream_t s, int pdl);
+// Both stages with the built-in (or overridden) plan: every entry point that
+// runs the whole layer goes through this, so they launch identical work.
+cudaError_t launch_layer(const GateUpArgs& ga, const DownArgs& da, void* h16, int32_t* hk,
+                         cudaStream_t s);
+
+// WD_OK for cudaSuccess (after also checking cudaGetLastError), else
+// WD_ERR_CUDA with the error's name kept for wd_last_error_string.
+wd_status cuda_status(cudaError_t e);
+
+// Raise `func`'s dynamic shared-memory limit to at least `bytes` on the current
+// device (once per kernel and device; thread-safe).
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
 
 cudaError_t launch_gate_up(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_gate_up_rowshare(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                     bool pdl);
-cudaError_t launch_gate_up_stream(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                                  bool pdl);
-bool gate_up_stream_supported(int B, int H, int I, int E, int K, int npw);
-cudaError_t launch_gate_up_mixed(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                                 bool pdl);
-bool gate_up_mixed_supported(int B, int H, int I, int E, int K, int npw);
 cudaError_t launch_gate_up_persist(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                    bool pdl);
 bool gate_up_persist_supported(int B, int H, int I, int E, int K);
-cudaError_t launch_gate_up_ring(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                                bool pdl);
-bool gate_up_ring_supported(int B, int H, int I, int E, int K, int stages);
-cudaError_t launch_gate_up_tma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
-                               bool pdl);
-bool gate_up_tma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStream_t stream,
                                bool pdl);
 bool gate_up_mma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
-cudaError_t launch_down_stream(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
-bool down_stream_supported(int B, int H, int I, int E, int K);
-cudaError_t launch_down_shared(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
-bool down_shared_supported(int B, int H, int I, int E, int K, int rpw);
-cudaError_t launch_down_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
-bool down_mma_supported(int B, int H, int I, int E, int K);
-cudaError_t launch_down_3d_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream,
-                               bool pdl);
-bool down_3d_mma_supported(int B, int H, int I, int E, int K);
-cudaError_t launch_down_expert_mma(const DownArgs& a, const DownPlan& p, cudaStream_t stream,
-                                   bool pdl);
-bool down_expert_mma_supported(int B, int H, int I, int E, int K);
+bool down_dimblock_supported(int B, int H, int I, int E, int K);
+// moe_down_dimblock's shape for I: consumer warps (returned), ring stages and
+// pairs per step; the wanted shape if all three are given and it fits, else
+// the built-in one; 0 warps if none fits.
+int down_dimblock_shape(int I, int want_nw, int want_spw, int want_p, int* S, int* P);
+cudaError_t launch_h_encode(const void* h, void* h16, int32_t* hk, int rows, int I,
+                            cudaStream_t stream, bool pdl);
+cudaError_t launch_down_dimblock(const DownArgs& a, const DownPlan& p, const void* h16,
+                                 const int32_t* hk, cudaStream_t stream, bool pdl);
 
 }  // namespace wd

@@ -5,12 +5,14 @@
 // plugin inside a host framework that owns every device allocation and forbids
 // new ones while it runs, or a latency-critical loop that cannot afford
 // cudaMalloc's possible implicit device synchronisation.  This entry point
-// keeps the layer's one scratch buffer (the BF16 intermediate h) in a
-// fixed-size array compiled into the library instead, so the caller passes
-// only inputs and outputs.
+// keeps the layer's scratch (the BF16 intermediate h and, for batches whose
+// tokens share experts, its FP16 re-encoding with per-row exponents) in a
+// fixed-size array compiled into the library instead, laid out exactly as a
+// workspace, so the caller passes only inputs and outputs and the call runs
+// the same kernels, in the same order, as wd_moe_decode.
 //
 // Costs of that choice, all documented in include/wd_moe.h:
-//   - every GPU that loads the library holds kNoAllocScratchBytes (1 MiB) for
+//   - every GPU that loads the library holds kNoAllocScratchBytes (2 MiB) for
 //     the life of the process, used or not;
 //   - all calls share the one array, so calls that may run at the same time on
 //     the GPU (different streams, no ordering between them) race on it;
@@ -24,7 +26,8 @@
 #include "../../include/wd_moe.h"
 #include "wd_launch.h"
 
-static constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB: h for B*K*I <= 524288
+// 2 MiB: the workspace layout of wd_moe_decode for up to B = 85 tokens at K = 8, I = 768
+static constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
 
 // The scratch itself.  In host code this name is only a stand-in for the
 // device object, not an address a kernel can use; the kernels get the address
@@ -72,23 +75,22 @@ extern "C" wd_status wd_moe_decode_no_alloc(const void* x, const int32_t* topk_i
   if (!aligned(x, 32) || !aligned(gate_up, 32) || !aligned(down, 32) || !aligned(topk_ids, 4) ||
       !aligned(topk_w, 4) || !aligned(out, 4))
     return WD_ERR_INVALID_ARG;
-  // h is BF16 [B, K, I]; it must fit the compiled-in scratch
-  if ((size_t)B * K * I * 2 > kNoAllocScratchBytes) return WD_ERR_WORKSPACE_TOO_SMALL;
+  // the workspace layout for this call must fit the compiled-in scratch
+  const size_t hb = wd::layer_scratch_h_bytes(B, K, I);
+  if (wd::layer_scratch_bytes(B, K, I) > kNoAllocScratchBytes) return WD_ERR_WORKSPACE_TOO_SMALL;
 
-  void* h = nullptr;
-  if (scratch_address(&h) != cudaSuccess) return WD_ERR_CUDA;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Nothing in the scratch needs clearing: the first kernel writes every h
-  // element the second kernel reads (zeros for out-of-range ids).  No error
-  // flag is kept: out-of-range ids contribute nothing and are not reported.
+  void* base = nullptr;
+  cudaError_t e = scratch_address(&base);
+  if (e != cudaSuccess) return wd::cuda_status(e);
+  uint8_t* b8 = static_cast<uint8_t*>(base);
+  void* h = b8 + 256;
+  // Nothing in the scratch needs clearing: every kernel writes each element
+  // the next one reads (zeros for out-of-range ids).  No error flag is kept:
+  // out-of-range ids contribute nothing and are not reported, and a bounded
+  // wait that runs out inside a kernel is not reported either.
   const wd::GateUpArgs ga{x, topk_ids, gate_up, gate_up_scale, h, nullptr, B, H, I, E, K};
-  const wd::GateUpPlan gp = wd::plan_gate_up_for(ga);
-  const int pdl = wd::pdl_mask_for(gp);
-  cudaError_t e = wd::launch_gate_up(ga, gp, s, (pdl & 1) != 0);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return WD_ERR_CUDA;
   const wd::DownArgs da{h, topk_ids, topk_w, down, down_scale, out, nullptr, B, H, I, E, K};
-  e = wd::launch_down(da, wd::plan_down_for(da), s, (pdl & 2) != 0);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  return e == cudaSuccess ? WD_OK : WD_ERR_CUDA;
+  return wd::cuda_status(wd::launch_layer(ga, da, b8 + 256 + hb,
+                                          reinterpret_cast<int32_t*>(b8 + 256 + 2 * hb),
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -20,9 +20,11 @@ normal), and each element is rounded to the nearest E4M3 value (ties to an even
 mantissa) after dividing by the scale, saturating at +-448.  The distance is the
 relative RMS error of y against the reference over all outputs of the batch.
 
-Test infrastructure: it reads the oracle (oracle/) and the generator (synth/)
-only.  `python tests/accuracy_study.py` prints the table quoted in the design
-notes.
+Test infrastructure: the study reads the oracle (oracle/) and the generator
+(synth/); gpu_column also runs this library's CUDA path on the same layer and
+measures its own error against the same reference (the test in
+tests/test_gpu_accuracy.py).  `python tests/accuracy_study.py [--gpu]` prints
+the table quoted in the design notes.
 """
 import os
 import sys
@@ -96,13 +98,30 @@ def _bf16_bits(v: np.ndarray) -> np.ndarray:
     return np.array([oracle.f64_to_bf16(float(t)) for t in v.ravel()], np.uint16).reshape(v.shape)
 
 
-def study(seed=1236, B=4, H=2048, I=768, E=128, K=8):
-    """Relative RMS error of y for the warp-decode and traditional activation
-    formats against the unrounded reference, on one seeded layer."""
+def layer_inputs(seed=1236, B=4, H=2048, I=768, E=128, K=8):
+    """One seeded layer: x (BF16 bits), ids, w and the MXFP8 weights."""
     gu, gus = synth.gate_up(seed, 0, E, H, I)
     dn, dns = synth.down(seed, 0, E, H, I)
     x = synth.x(seed, 0, B, H)
     ids, w = synth.route(seed, 0, B, E, K)
+    return x, ids, w, gu, gus, dn, dns
+
+
+def reference_y(x, ids, w, gu, gus, dn, dns, I, E):
+    """The unrounded reference output: FP64 throughout, h not rounded."""
+    _, h_f64, _ = oracle.gate_up(x, ids, gu, gus, I, E, with_f64=True)
+    return _down_f64(h_f64, ids, w, dn, dns, E)
+
+
+def rel_rms(y, y_ref):
+    """Relative RMS distance of y from y_ref over all outputs."""
+    return float(np.sqrt(np.mean((y - y_ref) ** 2)) / np.sqrt(np.mean(y_ref ** 2)))
+
+
+def study(seed=1236, B=4, H=2048, I=768, E=128, K=8):
+    """Relative RMS error of y for the warp-decode and traditional activation
+    formats against the unrounded reference, on one seeded layer."""
+    x, ids, w, gu, gus, dn, dns = layer_inputs(seed, B, H, I, E, K)
     # reference and warp decode share the first projection
     h_bits, h_f64, _ = oracle.gate_up(x, ids, gu, gus, I, E, with_f64=True)
     y_ref = _down_f64(h_f64, ids, w, dn, dns, E)
@@ -116,17 +135,45 @@ def study(seed=1236, B=4, H=2048, I=768, E=128, K=8):
     y_h_only = _down_f64(quantize_mxfp8(h_f64), ids, w, dn, dns, E)
 
     def rel(y):
-        return float(np.sqrt(np.mean((y - y_ref) ** 2)) / np.sqrt(np.mean(y_ref ** 2)))
+        return rel_rms(y, y_ref)
 
     e_wd, e_tr = rel(y_wd), rel(y_tr)
     return {"B": B, "rel_rms_warp_decode": e_wd, "rel_rms_traditional": e_tr,
             "ratio": e_tr / e_wd, "rel_rms_x_only": rel(y_x_only), "rel_rms_h_only": rel(y_h_only)}
 
 
+def gpu_column(seed=1236, B=4, H=2048, I=768, E=128, K=8, device="cuda:0"):
+    """This library's CUDA output (BF16, the built-in plan) on the same layer:
+    its relative RMS error against the unrounded reference, next to the
+    oracle's own output rounded to BF16 the same way (the error a perfect
+    implementation of this path would show)."""
+    import torch
+
+    import moe_decode_gate_gb300 as wd
+
+    x, ids, w, gu, gus, dn, dns = layer_inputs(seed, B, H, I, E, K)
+    y_ref = reference_y(x, ids, w, gu, gus, dn, dns, I, E)
+    dev = torch.device(device)
+    layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=K, max_batch=B, device=dev)
+    out = layer(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev),
+                torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev))
+    torch.cuda.synchronize(dev)
+    y_gpu = out.float().cpu().double().numpy()
+    y_oracle = oracle.bf16_bits_to_f64(oracle.moe_decode(x, ids, w, gu, gus, dn, dns, I, E))
+    return {"B": B, "rel_rms_gpu": rel_rms(y_gpu, y_ref), "rel_rms_oracle_bf16": rel_rms(y_oracle, y_ref),
+            "plan": wd.wd_moe_describe_plan(B, H, I, E, K)}
+
+
 if __name__ == "__main__":
-    print("| B | BF16 h (this path) | MXFP8 x and h | ratio | MXFP8 x only | MXFP8 h only |")
-    print("|---|---|---|---|---|---|")
-    for B in (1, 4, 8):
+    gpu = "--gpu" in sys.argv
+    print("| B | BF16 h (this path, FP64) | MXFP8 x and h | ratio | MXFP8 x only | MXFP8 h only |"
+          + (" CUDA path (BF16 out) | oracle, BF16 out |" if gpu else ""))
+    print("|---|---|---|---|---|---|" + ("---|---|" if gpu else ""))
+    for B in (1, 4, 8, 32):
         r = study(B=B)
-        print(f"| {B} | {r['rel_rms_warp_decode']:.3e} | {r['rel_rms_traditional']:.3e} "
-              f"| {r['ratio']:.1f} | {r['rel_rms_x_only']:.3e} | {r['rel_rms_h_only']:.3e} |")
+        line = (f"| {B} | {r['rel_rms_warp_decode']:.3e} | {r['rel_rms_traditional']:.3e} "
+                f"| {r['ratio']:.1f} | {r['rel_rms_x_only']:.3e} | {r['rel_rms_h_only']:.3e} |")
+        if gpu:
+            g = gpu_column(B=B)
+            line += f" {g['rel_rms_gpu']:.3e} | {g['rel_rms_oracle_bf16']:.3e} |"
+        print(line, flush=True)

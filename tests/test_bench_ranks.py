@@ -79,5 +79,7 @@ def test_reference_arm_line_on_rank_zero():
     assert r.returncode == 0, r.stderr
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == bench.UNIT
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and 1 <= cpu["cores"] <= (os.cpu_count() or 1)
+    assert cpu["hardware_concurrency"] == os.cpu_count() and cpu["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0

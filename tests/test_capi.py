@@ -16,7 +16,7 @@ from moe_decode_gate_gb300 import _native
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", f) for f in ("wd_moe.h", "wd_bench.h")]
 
-OK, INVALID, SHAPE, SMALL, CUDA, BADID = 0, 1, 2, 3, 4, 5
+OK, INVALID, SHAPE, SMALL, CUDA, BADID, TIMEOUT = 0, 1, 2, 3, 4, 5, 6
 
 
 def declared_symbols():
@@ -29,9 +29,10 @@ def declared_symbols():
 
 def test_headers_declare_the_expected_entry_points():
     names = set(declared_symbols())
-    for n in ("wd_moe_decode", "wd_moe_gate_up", "wd_moe_down", "wd_moe_workspace_size",
-              "wd_moe_workspace_init", "wd_moe_read_error_flag", "wd_status_string",
-              "wd_bench_copy", "wd_bench_read", "wd_bench_fill"):
+    for n in ("wd_moe_decode", "wd_moe_gate_up", "wd_moe_down", "wd_moe_down_workspace",
+              "wd_moe_workspace_size", "wd_moe_workspace_init", "wd_moe_read_error_flag",
+              "wd_status_string", "wd_moe_launches", "wd_bench_copy", "wd_bench_read",
+              "wd_bench_fill"):
         assert n in names
 
 
@@ -52,14 +53,16 @@ def test_library_was_built_for_sm_103a_only():
 def test_status_strings():
     for code, name in _native.STATUS_NAMES.items():
         assert wd.wd_status_string(code) == name
+    assert wd.wd_status_string(TIMEOUT) == "WD_ERR_PIPELINE_TIMEOUT"
     assert wd.wd_status_string(99) == "WD_ERR_UNKNOWN"
 
 
 def test_workspace_size():
-    # 256-byte flag slot + bf16 h [B, K, I] rounded up to 256 bytes
-    assert wd.wd_moe_workspace_size(1, 8, 768) == 256 + 12288
-    assert wd.wd_moe_workspace_size(32, 8, 768) == 256 + 32 * 8 * 768 * 2
-    assert wd.wd_moe_workspace_size(1, 1, 32) == 256 + 256
+    # 256-byte flag slot + bf16 h [B, K, I] + its FP16 re-encoding [B, K, I] +
+    # int32 exponents [B, K], each rounded up to 256 bytes
+    assert wd.wd_moe_workspace_size(1, 8, 768) == 256 + 2 * 12288 + 256
+    assert wd.wd_moe_workspace_size(32, 8, 768) == 256 + 2 * 32 * 8 * 768 * 2 + 1024
+    assert wd.wd_moe_workspace_size(1, 1, 32) == 256 + 256 + 256 + 256
     assert wd.wd_moe_workspace_size(0, 8, 768) == 0
     assert wd.wd_moe_workspace_size(1, -1, 768) == 0
 
@@ -84,7 +87,7 @@ def _decode(x=A32, ids=A32, w=A32, gu=A32, gus=A32, dn=A32, dns=A32, out=A32, ws
     (dict(x=A32 + 16), INVALID), (dict(gu=A32 + 16), INVALID), (dict(dn=A32 + 8), INVALID),
     (dict(ids=A32 + 2), INVALID), (dict(w=A32 + 1), INVALID), (dict(out=A32 + 2), INVALID),
     (dict(ws=A32 + 128), INVALID),
-    (dict(ws_bytes=256 + 12287), SMALL), (dict(ws_bytes=0), SMALL),
+    (dict(ws_bytes=256 + 2 * 12288 + 255), SMALL), (dict(ws_bytes=0), SMALL),
 ])
 def test_decode_rejects_bad_arguments_on_the_host(kw, status):
     assert _decode(**kw) == status
@@ -101,6 +104,16 @@ def test_split_kernels_reject_bad_arguments():
     assert lib.wd_moe_down(A32 + 16, A32, A32, A32, A32, A32, None, 1, 2048, 768, 128, 8, None) == INVALID
     assert lib.wd_moe_down(A32, A32, None, A32, A32, A32, None, 1, 2048, 768, 128, 8, None) == INVALID
     assert lib.wd_moe_down(A32, A32, A32, A32, A32, A32, None, 1, 2048, 100, 128, 8, None) == SHAPE
+    # down with a workspace: aligned h and workspace, and a large enough workspace
+    ws = wd.wd_moe_workspace_size(32, 8, 768)
+    assert lib.wd_moe_down_workspace(A32 + 16, A32, A32, A32, A32, A32, A32, ws,
+                                     32, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_down_workspace(A32, A32, A32, A32, A32, A32, A32 + 64, ws,
+                                     32, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_down_workspace(A32, A32, A32, A32, A32, A32, None, ws,
+                                     32, 2048, 768, 128, 8, None) == INVALID
+    assert lib.wd_moe_down_workspace(A32, A32, A32, A32, A32, A32, A32, ws - 1,
+                                     32, 2048, 768, 128, 8, None) == SMALL
 
 
 def test_workspace_calls_reject_bad_arguments():
@@ -129,7 +142,11 @@ def test_last_error_string_starts_empty():
 
 
 def test_launch_count():
-    assert wd.wd_moe_launches_per_call() == 2
+    assert wd.wd_moe_launches_per_call() == 3
+    wd.wd_moe_set_plan(None)
+    q = dict(H=2048, I=768, E=128, K=8)
+    assert [wd.wd_moe_launches(B, **q) for B in (1, 2, 4, 8, 16, 32, 64)] == [2, 2, 2, 2, 3, 3, 2]
+    assert wd.wd_moe_launches(0, **q) == 0
 
 
 def test_built_in_plan_by_batch():
@@ -137,35 +154,37 @@ def test_built_in_plan_by_batch():
     wd.wd_moe_set_plan(None)
     q = dict(H=2048, I=768, E=128, K=8)
     assert wd.wd_moe_describe_plan(1, **q) == \
-        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6> pdl=3"
+        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6> pdl=3 launches=2"
     assert wd.wd_moe_describe_plan(2, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3> pdl=3"
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3> pdl=3 launches=2"
     assert wd.wd_moe_describe_plan(4, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1> pdl=3"
-    for B in (8, 16, 32):  # tokens share experts: tensor-core gate/up, down not overlapped
+        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1> pdl=3 launches=2"
+    # tokens share experts: tensor-core gate/up; from B*K >= E on, each routed
+    # down row is read once for all of its pairs
+    assert wd.wd_moe_describe_plan(8, **q) == \
+        "gate_up=moe_gate_up_mma<8,0> down=moe_down_3d_batched<4,1> pdl=1 launches=2"
+    for B in (16, 32):
         assert wd.wd_moe_describe_plan(B, **q) == \
-            "gate_up=moe_gate_up_mma<8,0> down=moe_down_3d_batched<4,1> pdl=1"
-    # H above the tensor-core kernel's limit: the CUDA-core persistent kernel
-    assert wd.wd_moe_describe_plan(32, 4096, 768, 128, 8).startswith("gate_up=moe_gate_up_persist<2,1>")
-    # B*K above the persistent kernel's routing tables: the shared-row kernel
-    assert wd.wd_moe_describe_plan(64, **q).startswith("gate_up=moe_gate_up_rowshare<2,2>")
-    wd.wd_moe_set_plan("gu=mma,dn=emma:12")
+            "gate_up=moe_gate_up_mma<8,0> down=moe_down_dimblock<4,2,6> pdl=7 launches=3"
+    # H above the tensor-core gate/up kernel's limit: the CUDA-core persistent kernel
+    assert wd.wd_moe_describe_plan(32, 4096, 768, 128, 8).startswith(
+        "gate_up=moe_gate_up_persist<2,1> down=moe_down_dimblock<4,2,6>")
+    # B*K above the persistent kernels' routing tables: shared-row gate/up, batched down
+    assert wd.wd_moe_describe_plan(64, **q) == \
+        "gate_up=moe_gate_up_rowshare<2,2> down=moe_down_3d_batched<4,1> pdl=3 launches=2"
+    # I not a multiple of 128: no tensor-map slabs for the down rows
+    assert "down=moe_down_3d_batched<4,1>" in wd.wd_moe_describe_plan(32, 2048, 800, 128, 8)
+    wd.wd_moe_set_plan("gu=mma,dn=4:1,pdl=1")
     try:
         assert wd.wd_moe_describe_plan(32, **q) == \
-            "gate_up=moe_gate_up_mma<8,0> down=moe_down_expert_mma<1,12> pdl=1"
+            "gate_up=moe_gate_up_mma<8,0> down=moe_down_3d_batched<4,1> pdl=1 launches=2"
     finally:
         wd.wd_moe_set_plan(None)
-    # a shape the expert-step down kernel does not take (B > 64) keeps the built-in down
-    wd.wd_moe_set_plan("dn=emma")
+    # the shared-row down on request even where tokens rarely share experts
+    wd.wd_moe_set_plan("dn=dimblock:3:3:5")
     try:
-        assert wd.wd_moe_describe_plan(32, **q).endswith("down=moe_down_expert_mma<1,0> pdl=1")
+        assert wd.wd_moe_describe_plan(2, **q).endswith("down=moe_down_dimblock<3,3,5> pdl=7 launches=3")
         assert "down=moe_down_3d_batched<4,1>" in wd.wd_moe_describe_plan(128, 2048, 768, 128, 2)
-    finally:
-        wd.wd_moe_set_plan(None)
-    wd.wd_moe_set_plan("gu=batched:1:2,dn=shared:4")
-    try:
-        assert wd.wd_moe_describe_plan(32, **q) == \
-            "gate_up=moe_gate_up_3d_batched<1,2> down=moe_down_shared<4,0> pdl=3"
     finally:
         wd.wd_moe_set_plan(None)
     lib = wd.lib()
@@ -179,16 +198,17 @@ def test_plan_override_parser():
     lib = wd.lib()
     assert lib.wd_moe_set_plan(b"gu=rowshare:2:1,dn=4:1,rowshare_min_b=4") == OK
     assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
-    assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=persist:4:1") == OK
-    assert lib.wd_moe_set_plan(b"gu=persist:1:1,dn=shared:2") == OK
-    assert lib.wd_moe_set_plan(b"gu=tma,dn=4:1") == OK
-    assert lib.wd_moe_set_plan(b"gu=ring:2") == OK
+    assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=4:1") == OK
     assert lib.wd_moe_set_plan(b"gu=mma,pdl=3") == OK
     assert lib.wd_moe_set_plan(b"gu=mma:2,pdl=0") == OK
-    assert lib.wd_moe_set_plan(b"gu=mma,dn=emma") == OK
-    assert lib.wd_moe_set_plan(b"dn=emma:3,pdl=3") == OK
-    assert lib.wd_moe_set_plan(b"dn=emma:0:2") == OK
-    assert lib.wd_moe_set_plan(b"pdl=4") == INVALID
+    assert lib.wd_moe_set_plan(b"gu=mma:2:16,dn=dimblock") == OK
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6,pdl=7") == OK
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2") == INVALID
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6:1") == INVALID
+    # kernels that are no longer part of the library
+    for gone in (b"gu=tma", b"gu=ring:2", b"dn=emma", b"dn=shared:2", b"dn=persist:4:1"):
+        assert lib.wd_moe_set_plan(gone) == INVALID
+    assert lib.wd_moe_set_plan(b"pdl=8") == INVALID
     assert lib.wd_moe_set_plan(b"nonsense") == INVALID
     assert lib.wd_moe_set_plan(b"dn=2") == INVALID
     assert lib.wd_moe_set_plan(None) == OK

@@ -230,31 +230,17 @@ PLANS = [
     "gu=rowshare:2:1,dn=2:2",
     "gu=rowshare:2:2,dn=1:6",
     "gu=batched:1:1,dn=1:4",
-    "gu=stream:2:2,dn=stream:8",
-    "gu=stream:1:2,dn=stream:3",
-    "gu=stream:3:3,dn=stream:2",
-    "gu=mixed:1:2,dn=4:1",
-    "gu=mixed:3:2,dn=2:3",
-    "gu=mixed:2:2,dn=2:2",
-    "gu=persist:2:2,dn=persist:4:1",
-    "gu=persist:2:1,dn=persist:2:1",
-    "gu=persist:1:1,dn=persist:2:3",
-    "gu=persist:1:2,dn=4:1",
-    "gu=persist:2:2,dn=persist:1:6",
-    "gu=persist:2:2,dn=shared:4",
-    "gu=ring:2,dn=4:1",
-    "gu=ring:3,dn=2:3",
-    "gu=tma,dn=4:1",
-    "gu=batched:2:1,dn=shared:2",
+    "gu=persist:2:2,dn=4:1",
+    "gu=persist:2:1,dn=2:2",
+    "gu=persist:1:1,dn=2:3",
+    "gu=persist:1:2,dn=dimblock",
     "gu=mma,dn=4:1",
-    "gu=mma,dn=mma",
     "gu=mma:2:16,dn=4:1",
-    "gu=mma,dn=3dmma",
-    "gu=batched:2:1,dn=3dmma",
-    "gu=persist:2:1,dn=mma:2",
-    "gu=mma,dn=emma",
-    "gu=persist:2:1,dn=emma:8",
-    "gu=mma,dn=emma:0:2",
+    "gu=mma,dn=dimblock",
+    "gu=mma,dn=dimblock:2:1:3",
+    "gu=mma,dn=dimblock:5:2:4",
+    "gu=mma,dn=dimblock:1:1:1",
+    "gu=batched:2:1,dn=dimblock,pdl=0",
 ]
 
 PLAN_SHAPES = [
@@ -291,15 +277,10 @@ def test_every_kernel_instance_matches_the_oracle(cuda_device, plan_reset, B, H,
 
 
 @pytest.mark.parametrize("plan", ["gu=rowshare:2:2,rowshare_min_b=1,dn=2:3",
-                                  "gu=stream:2:3,dn=stream:8",
-                                  "gu=persist:2:2,dn=persist:4:1",
-                                  "gu=persist:2:2,dn=shared:4",
-                                  "gu=ring:2,dn=4:1",
-                                  "gu=tma,dn=4:1",
+                                  "gu=persist:2:2,dn=4:1",
                                   "gu=mma,dn=4:1",
-                                  "gu=batched:2:1,dn=mma",
-                                  "gu=batched:2:1,dn=3dmma",
-                                  "gu=batched:2:1,dn=emma"])
+                                  "gu=batched:2:1,dn=dimblock",
+                                  "gu=mma,dn=dimblock"])
 def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     wd.wd_moe_set_plan(plan)
     xs, ids, w, gu, gus, dn, dns = _random_case(17, 9, 512, 128, 8, 3)
@@ -311,25 +292,6 @@ def test_routing_table_kernels_handle_bad_ids(cuda_device, plan_reset, plan):
     assert not got_h[0, 1].any() and not got_h[4, 0].any() and not got_h[8, 2].any()
     compare(got_h.reshape(-1, 128), want_h.reshape(-1, 128), "rowshare bad ids h")
     compare(got, want, "rowshare bad ids")
-
-
-@pytest.mark.parametrize("plan", ["gu=mixed:1:2", "gu=mixed:3:2", "gu=mixed:2:2"])
-def test_fp16_product_path_keeps_tokens_fp16_cannot_hold_exact(cuda_device, plan_reset, plan):
-    """The mixed-precision gate/up kernel multiplies in FP16 only for tokens
-    whose BF16 activations are all exactly representable in FP16; the others
-    must take the FP32 path.  Tokens here: ordinary; one tiny (1e-30) element;
-    one element above the FP16 range; all zeros; an element at 2^-17 (still
-    exact); an element at 2^-18 (not exact)."""
-    wd.wd_moe_set_plan(plan)
-    xs, ids, w, gu, gus, dn, dns = _random_case(21, 6, 1024, 256, 8, 3)
-    xf = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).float()
-    xf[1, 17] = 1e-30
-    xf[2, 900] = 7.0e4
-    xf[3, :] = 0.0
-    xf[4, 5] = 2.0 ** -17
-    xf[5, 1000] = 2.0 ** -18
-    xs = xf.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"{plan} fp16 boundary tokens")
 
 
 # moe_gate_up_mma: B*K <= 256, H % 512 == 0, H <= 2048, I % 16 == 0.  Shapes:
@@ -420,12 +382,15 @@ def test_gate_up_mma_special_scale_codes(cuda_device, plan_reset):
     assert err <= 1e-2 * np.abs(want).max() + 2e-3
 
 
-# moe_down_mma: B <= 64, B*K <= 256, H % 16 == 0, I % 128 == 0.  Shapes: the
-# full-size layer at B = 8..64 with every routing pattern (fixed: 32 pairs per
-# expert, four groups of 8; disjoint: 2 per expert), two CTAs (H = 32), I = 128
-# (one block per consumer warp and none for the others), ~13 pairs per expert
-# (a second, partly empty group), duplicate-prone K == E, and a single token.
-DN_MMA_SHAPES = [
+# moe_down_dimblock (after moe_h_encode): B <= 64, B*K <= 256, H % 16 == 0,
+# I % 128 == 0, I <= 2048.  Shapes: the full-size layer at B = 8..64 with every
+# routing pattern (fixed: 32 pairs per expert, six steps of up to 6; disjoint:
+# 2 per expert), two CTAs (H = 32) and six (H = 96), I = 128 (four blocks per
+# step), I = 2048 (a two-stage ring, one consumer warp), ~13 pairs per expert
+# (a third, partly empty step), duplicate-prone K == E, and a single token;
+# each with the built-in shape (4 consumer warps, 2 stages each, 6 pairs per
+# step) and with 1 warp x 2 stages x 6 pairs, 2 x 2 x 8 and 3 x 3 x 5.
+DN_SHAPES = [
     (8, 2048, 768, 128, 8, "uniform"),
     (16, 2048, 768, 128, 8, "uniform"),
     (32, 2048, 768, 128, 8, "uniform"),
@@ -434,36 +399,39 @@ DN_MMA_SHAPES = [
     (32, 2048, 768, 128, 8, "disjoint"),
     (64, 2048, 768, 128, 4, "uniform"),
     (2, 32, 128, 2, 2, "uniform"),
+    (3, 96, 256, 3, 3, "uniform"),
     (40, 1024, 128, 6, 2, "uniform"),
+    (7, 512, 2048, 6, 6, "uniform"),
     (3, 512, 384, 3, 3, "uniform"),
     (1, 2048, 768, 128, 8, "uniform"),
 ]
 
 
-@pytest.mark.parametrize("plan,kernel", [("dn=mma", "moe_down_mma<"),
-                                         ("dn=emma", "moe_down_expert_mma<"),
-                                         ("dn=emma:0:2", "moe_down_expert_mma<")])
-@pytest.mark.parametrize("B,H,I,E,K,route", DN_MMA_SHAPES)
-def test_down_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route, plan, kernel):
+@pytest.mark.parametrize("plan", ["dn=dimblock", "dn=dimblock:1:2:6", "dn=dimblock:2:2:8",
+                                  "dn=dimblock:3:3:5"])
+@pytest.mark.parametrize("B,H,I,E,K,route", DN_SHAPES)
+def test_down_dimblock_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route, plan):
     wd.wd_moe_set_plan(plan)
-    assert f"down={kernel}" in wd.wd_moe_describe_plan(B, H, I, E, K)
+    assert "down=moe_down_dimblock<" in wd.wd_moe_describe_plan(B, H, I, E, K)
     xs, ids, w, gu, gus, dn, dns = _random_case(1100 + B + H + I + E, B, H, I, E, K, route=route)
     check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"{plan} B={B} H={H} I={I} {route}")
 
 
 def _down_alone(dev, h_bits, ids, w, dn, dns, H, E):
+    """The down stage alone, on a given h, through wd_moe_down_workspace."""
     B, K, I = h_bits.shape
     want = oracle.down(h_bits, ids, w, dn, dns, H, E)
     out = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
-    flag = torch.zeros(1, dtype=torch.int32, device=dev)
-    wd.wd_moe_down(to_dev_bf16(h_bits, dev), to_dev(ids, dev), to_dev(w, dev), to_dev(dn, dev),
-                   to_dev(dns, dev), out, error_flag=flag)
+    ws = torch.empty(wd.wd_moe_workspace_size(B, K, I), dtype=torch.uint8, device=dev)
+    wd.wd_moe_workspace_init(ws)
+    wd.wd_moe_down_workspace(to_dev_bf16(h_bits, dev), to_dev(ids, dev), to_dev(w, dev),
+                             to_dev(dn, dev), to_dev(dns, dev), out, ws)
     torch.cuda.synchronize()
-    return from_dev_bf16(out), want, int(flag.item())
+    return from_dev_bf16(out), want, wd.wd_moe_read_error_flag(ws)
 
 
-@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma", "dn=emma"])
-def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset, plan):
+@pytest.mark.parametrize("plan", ["dn=dimblock", "dn=4:1"])
+def test_down_h_range_and_duplicates(cuda_device, plan_reset, plan):
     """h rows are re-encoded per (token, slot) as FP16 times a power of two:
     ordinary rows, rows of magnitude 1e-20 and 1e+20, an all-zero row, BF16
     subnormals only, a row spanning 1e-12 .. 1e+3; a token routed twice to one
@@ -489,8 +457,8 @@ def test_down_mma_h_range_and_duplicates(cuda_device, plan_reset, plan):
         compare(got[t:t + 1], want[t:t + 1], f"{plan} token {t}")
 
 
-@pytest.mark.parametrize("plan", ["dn=mma", "dn=3dmma", "dn=emma"])
-def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan):
+@pytest.mark.parametrize("plan", ["dn=dimblock", "dn=4:1"])
+def test_down_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan):
     """E8M0 codes far from 1 (2^-40 .. 2^+19), 0 (2^-127) on a whole row and 255
     (NaN) on one block; an out-of-range id contributes nothing and is flagged."""
     wd.wd_moe_set_plan(plan)
@@ -505,7 +473,7 @@ def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan)
     dns[1, 20, 2] = 255    # expert 1, output dim 20: one NaN block
     h = oracle.gate_up(xs, ids, gu, gus, I, E)
     got_b, want_b, flag = _down_alone(cuda_device, h, ids, w, dn, dns, H, E)
-    assert flag == 1
+    assert flag == wd.FLAG_BAD_EXPERT_ID
     got, want = bf16_bits_to_f64(got_b), bf16_bits_to_f64(want_b)
     assert np.array_equal(np.isnan(got), np.isnan(want))
     assert np.isnan(want[:, 20]).sum() == 2  # tokens 0 and 1 route expert 1
@@ -515,28 +483,35 @@ def test_down_mma_special_scale_codes_and_bad_ids(cuda_device, plan_reset, plan)
     assert err <= 1e-2 * np.abs(want).max() + 2e-3
 
 
-# moe_down_3d_mma: H % 16 == 0, I % 256 == 0, I <= 1024, K <= 32.  Shapes:
-# the full-size layer at B = 1..64 with every routing pattern, two 16-dim
-# groups (H = 32), I = 1024 (four 8-block passes per routed row) and I = 256
-# (one), and K == E.
-DN_3DMMA_SHAPES = [
-    (1, 2048, 768, 128, 8, "uniform"),
-    (8, 2048, 768, 128, 8, "uniform"),
-    (32, 2048, 768, 128, 8, "uniform"),
-    (32, 2048, 768, 128, 8, "zipf"),
-    (32, 2048, 768, 128, 8, "fixed"),
-    (32, 2048, 768, 128, 8, "disjoint"),
-    (64, 2048, 768, 128, 4, "uniform"),
-    (5, 32, 512, 4, 2, "uniform"),
-    (7, 2048, 1024, 6, 6, "uniform"),
-    (6, 256, 256, 5, 1, "uniform"),
-    (3, 512, 256, 3, 3, "uniform"),
-]
+def test_down_workspace_matches_the_layer(cuda_device, plan_reset):
+    """wd_moe_down_workspace on the layer's own h gives the layer's output, bit
+    for bit (the same kernels in the same order)."""
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    gu, gus, dn, dns = weights(wl)
+    for B in (4, 16):
+        xs, ids, w = inputs(wl, B)
+        layer = wd.MoEDecodeLayer(gu, gus, dn, dns, K=wl.K, max_batch=B, device=cuda_device)
+        ids_d, w_d = to_dev(ids, cuda_device), to_dev(w, cuda_device)
+        out = layer(to_dev_bf16(xs, cuda_device), ids_d, w_d)
+        h = layer.workspace[256:256 + B * wl.K * wl.I * 2].view(torch.bfloat16).view(B, wl.K, wl.I)
+        h = h.clone()
+        out2 = torch.empty_like(out)
+        ws = torch.empty(wd.wd_moe_workspace_size(B, wl.K, wl.I), dtype=torch.uint8, device=cuda_device)
+        wd.wd_moe_workspace_init(ws)
+        wd.wd_moe_down_workspace(h, ids_d, w_d, layer.down, layer.down_scale, out2, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16)), f"B={B}"
 
 
-@pytest.mark.parametrize("B,H,I,E,K,route", DN_3DMMA_SHAPES)
-def test_down_3d_mma_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route):
-    wd.wd_moe_set_plan("dn=3dmma")
-    assert "down=moe_down_3d_mma" in wd.wd_moe_describe_plan(B, H, I, E, K)
-    xs, ids, w, gu, gus, dn, dns = _random_case(1300 + B + H + I + E, B, H, I, E, K, route=route)
-    check_layer(cuda_device, xs, ids, w, gu, gus, dn, dns, f"dn=3dmma B={B} H={H} I={I} {route}")
+def test_error_flag_bits_map_to_statuses(cuda_device):
+    """The flag read reports the raw mask and the status of its worst bit: a
+    bounded wait that ran out (bit 1) wins over a skipped expert id (bit 0).
+    The bits are planted with a device fill, no kernel has to fail."""
+    ws = torch.empty(wd.wd_moe_workspace_size(1, 8, 768), dtype=torch.uint8, device=cuda_device)
+    wd.wd_moe_workspace_init(ws)
+    flag_word = ws[:4].view(torch.int32)
+    for planted, status in ((0, 0), (1, 5), (2, 6), (3, 6)):
+        flag_word.fill_(planted)
+        mask, st = wd.wd_moe_read_error_flag(ws, with_status=True)
+        assert (mask, wd.wd_status_string(st)) == (planted, wd.wd_status_string(status))
+        assert wd.wd_moe_read_error_flag(ws) == 0  # cleared by the read

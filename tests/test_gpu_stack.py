@@ -1,7 +1,8 @@
 """GPU parity of the 48-layer decode stack, in the launch configuration bench.py
 times: the stack's device-resident weights, one CUDA graph of all layers'
-launches (programmatic dependent launch between the two kernels of a layer),
-the built-in launch plan, B=32.
+launches (at B=32: moe_gate_up_mma, moe_h_encode and moe_down_dimblock per
+layer, each a programmatic dependent of the one before), the built-in launch
+plan, B=32.
 
 Tokens are independent through the stack (there is no attention), so the
 oracle follows a few sampled tokens through every layer on its own, with only
