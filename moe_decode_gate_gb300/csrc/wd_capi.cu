@@ -26,14 +26,15 @@ namespace wd {
 // call) overrides the choice for tuning sweeps and tests:
 //   "gu=batched:<npw>:<cpl>" | "gu=rowshare:<npw>:<sbw>" | "gu=persist:<npw>:<prefetch+1>" |
 //   "gu=mma[:<stages>[:<consumer warps, 8 or 16>]]",
-//   "dn=<rpw>:<qpl>" | "dn=dimblock[:<consumer warps>:<stages per warp>:<pairs per step>]",
+//   "dn=<rpw>:<qpl>" |
+//   "dn=dimblock[:<step groups>:<stages per group>:<pairs per step>:<warps per step>]",
 //   "rowshare_min_b=<B>", "pdl=<mask>" (bit i: launch i of the call may overlap
 //   the launch before it), comma-separated; "" or NULL restores the defaults.
 namespace {
 
 struct PlanOverride {
   int gu_variant = -1, gu_npw = 0, gu_cpl = 0;
-  int dn_variant = -1, dn_rpw = 0, dn_qpl = 0, dn_pairs = 0;
+  int dn_variant = -1, dn_rpw = 0, dn_qpl = 0, dn_pairs = 0, dn_split = 0;
   int rowshare_min_b = 16;  // shared-row kernel where the persistent one does not apply
   int pdl_mask = -1;        // -1: by the plan (pdl_mask_for)
 };
@@ -71,17 +72,19 @@ bool parse_plan(const char* spec, PlanOverride* out) {
         p.gu_variant = kGateUpRowShare;
         p.gu_npw = a;
         p.gu_cpl = b;
-      } else if (int c = 0, n = 0;
-                 sscanf(tok, "dn=dimblock:%d:%d:%d%n", &a, &b, &c, &n) == 3 && tok[n] == 0) {
+      } else if (int c = 0, d = 0, n = 0;
+                 sscanf(tok, "dn=dimblock:%d:%d:%d:%d%n", &a, &b, &c, &d, &n) == 4 && tok[n] == 0) {
         p.dn_variant = kDownDimBlock;
         p.dn_rpw = a;
         p.dn_qpl = b;
         p.dn_pairs = c;
+        p.dn_split = d;
       } else if (strcmp(tok, "dn=dimblock") == 0) {
         p.dn_variant = kDownDimBlock;
         p.dn_qpl = 0;
         p.dn_rpw = 0;
         p.dn_pairs = 0;
+        p.dn_split = 0;
       } else if (sscanf(tok, "dn=%d:%d", &a, &b) == 2) {
         p.dn_variant = kDownBatched;
         p.dn_rpw = a;
@@ -144,23 +147,23 @@ DownPlan batched_down_plan(int B, int I, int K) {
   return DownPlan{2, per_lane >= 3 ? 3 : (per_lane >= 2 ? 2 : 1), kDownBatched};
 }
 
-static DownPlan dimblock_plan(int I, int nw, int spw, int pairs) {
-  int S = 0, P = 0;
-  const int NW = down_dimblock_shape(I, nw, spw, pairs, &S, &P);
-  return DownPlan{NW, S, kDownDimBlock, P};
+static DownPlan dimblock_plan(int I, int ns, int spg, int pairs, int split) {
+  int S = 0, P = 0, G = 0;
+  const int NS = down_dimblock_shape(I, ns, spg, pairs, split, &S, &P, &G);
+  return DownPlan{NS, S, kDownDimBlock, P, G};
 }
 
 DownPlan plan_down(int B, int H, int I, int K, int E) {
   const PlanOverride& o = plan_override();
   if (o.dn_variant == kDownBatched) return batched_down_plan(B, I, K);
   if (o.dn_variant == kDownDimBlock && down_dimblock_supported(B, H, I, E, K))
-    return dimblock_plan(I, o.dn_rpw, o.dn_qpl, o.dn_pairs);
+    return dimblock_plan(I, o.dn_rpw, o.dn_qpl, o.dn_pairs, o.dn_split);
   // built-in: once most routed experts serve several (token, slot) pairs
   // (B*K >= E: B >= 16 at K = 8, E = 128), read each routed row once for all
   // of them; before that, one warp per (token, output dims) (measured on
   // GB300: B = 8 59.1 vs 62.7 us/layer, B = 16 equal, B = 32 140.1 vs 124.3)
   if (o.dn_variant < 0 && B * K >= E && down_dimblock_supported(B, H, I, E, K))
-    return dimblock_plan(I, 0, 0, 0);
+    return dimblock_plan(I, 0, 0, 0, 0);
   return batched_down_plan(B, I, K);
 }
 
@@ -385,9 +388,9 @@ wd_status wd_moe_down_encoded(const void* h16, const int32_t* hk, const int32_t*
                        B, H, I, E, K};
   wd::DownPlan p = wd::plan_down(B, H, I, K, E);
   if (p.variant != wd::kDownDimBlock) {
-    int S = 0, P = 0;
-    const int NW = wd::down_dimblock_shape(I, 0, 0, 0, &S, &P);
-    p = wd::DownPlan{NW, S, wd::kDownDimBlock, P};
+    int S = 0, P = 0, G = 0;
+    const int NS = wd::down_dimblock_shape(I, 0, 0, 0, 0, &S, &P, &G);
+    p = wd::DownPlan{NS, S, wd::kDownDimBlock, P, G};
   }
   return cuda_status(wd::launch_down_dimblock(a, p, h16, hk,
                                               reinterpret_cast<cudaStream_t>(stream), false));
@@ -475,9 +478,9 @@ wd_status wd_moe_describe_plan(int B, int H, int I, int E, int K, char* buf, siz
   const char* gn = (g.variant >= 0 && g.variant < ngu) ? gu_names[g.variant] : "?";
   const char* dn = (d.variant >= 0 && d.variant < ndn) ? dn_names[d.variant] : "?";
   if (d.variant == wd::kDownDimBlock)
-    snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d,%d> pdl=%d launches=%d", gn, g.npw,
-             g.cpl, dn, d.rpw, d.qpl / (d.rpw > 0 ? d.rpw : 1), d.pairs, wd::pdl_mask_for(g, d),
-             wd::launches_for(d));
+    snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d,%d,%d> pdl=%d launches=%d", gn, g.npw,
+             g.cpl, dn, d.rpw, d.qpl / (d.rpw > 0 ? d.rpw : 1), d.pairs, d.split,
+             wd::pdl_mask_for(g, d), wd::launches_for(d));
   else
     snprintf(buf, bytes, "gate_up=%s<%d,%d> down=%s<%d,%d> pdl=%d launches=%d", gn, g.npw, g.cpl,
              dn, d.rpw, d.qpl, wd::pdl_mask_for(g, d), wd::launches_for(d));

@@ -33,36 +33,36 @@
 //     the same amount of work.  CTA c starts its walk at its own point of the
 //     step list (c / gridDim of the way in) and wraps around, so the CTAs read
 //     different experts' rows at any moment;
-//   - two producer warps (even and odd stages: a step's copies cost the
-//     issuing thread a few hundred cycles) stream each step into the ring: the
-//     expert's 16 down rows (one 3-D tensor-map copy, 128-byte swizzled so
-//     that the MMA fragment reads of 8 rows hit 8 different 16-byte bank
-//     groups), their scale codes (one bulk copy of 16 x I/32 bytes) and the
-//     pairs' FP16 h rows (one bulk copy per pair, issued by as many lanes).
-//     The first S steps' weights are requested before the kernel waits for
-//     the grid that writes h, so the ring fills while the previous kernels
-//     drain;
-//   - NW consumer warps; warp w takes the steps w, w + NW, ... whole and owns
-//     the S / NW stages they use (built-in: 4 warps, 2 stages each, up to 6
-//     pairs per step).  Per 32-column block: two k16 MMAs
-//     (E4M3 -> FP16 straight into the A fragments, exact) from a zero tile,
-//     then the tile times the rows' power-of-two block scales (decoded through
-//     a 256-entry table) into FP32 sums.  A step is I / 32 independent block
-//     chains, enough work in flight for one warp per scheduler;
-//   - a step's sums are final for its pairs: each lane stores them, unscaled,
-//     into the per-slot result table [B*K][16] (one writer per entry, plain
-//     stores);
+//   - two producer threads (one per producer warp, even and odd stages)
+//     stream each step's weights into an S-stage ring: the expert's 16 down
+//     rows (one 3-D tensor-map copy, 128-byte swizzled so that the MMA
+//     fragment reads of 8 rows hit 8 different 16-byte bank groups) and their
+//     scale codes (one bulk copy of 16 x I/32 bytes).  The weights do not
+//     depend on the previous kernels, so the ring fills while they drain;
+//   - NS step groups of G consumer warps; group q takes the steps q, q + NS,
+//     ... and owns the S / NS stages they use; each warp of a group does its
+//     part of I (built-in at I = 768: 4 groups of 2 warps with 12 blocks each,
+//     3 stages per group, up to 8 pairs per step).  Before waiting for its
+//     stage, each lane requests its B fragments from global memory: the FP16
+//     h row of its pair (L2-resident, written by moe_h_encode), 16 bytes per
+//     block, so that the h latency overlaps the weights' and h takes no room
+//     in the ring.  Per 32-column block: two k16 MMAs (E4M3 -> FP16 straight
+//     into the A fragments, exact) from a zero tile, then the tile times the
+//     rows' power-of-two block scales (decoded through a 256-entry table)
+//     into FP32 sums;
+//   - a warp's sums over its part of I are final for the step's pairs: each
+//     lane stores them, unscaled, into its part's per-slot result table
+//     [B*K][16] (one writer per entry, plain stores);
 //   - at the end every output is y = sum over k = 0..K-1 of the slot's result
-//     times w * 2^-k (the routing weight and the slot's re-encoding exponent),
-//     then one BF16 store.
+//     (its parts added in order) times w * 2^-k (the routing weight and the
+//     slot's re-encoding exponent), then one BF16 store.
 //
-// A stage is refilled only after its consumer warp released it and every
-// stage is used by one consumer warp (NW divides S) and one producer warp, in
+// A stage is refilled only after its group's warps released it and every
+// stage is used by one step group (NS divides S) and one producer warp, in
 // step order, so no wait can be more than one phase behind: the mbarrier
-// phase parity is unambiguous.  Every wait is bounded
-// (wd_pipeline.cuh); a warp whose wait runs out raises bit 1 of the error flag
-// and stops; the producers wait (bounded) for their last copies before
-// exiting.
+// phase parity is unambiguous.  Every wait is bounded (wd_pipeline.cuh); a
+// warp whose wait runs out raises bit 1 of the error flag and stops; the
+// producers wait (bounded) for their last copies before exiting.
 #include "wd_launch.h"
 #include "wd_mma.cuh"
 #include "wd_persist.cuh"
@@ -71,8 +71,9 @@ namespace wd {
 
 namespace {
 
-constexpr int kDMaxStages = 16;    // ring stages (stages per consumer warp x consumer warps)
-constexpr int kDMaxWarps = 8;      // consumer warps
+constexpr int kDMaxStages = 16;    // ring stages (stages per step group x step groups)
+constexpr int kDMaxWarps = 8;      // consumer warps (step groups x warps per step)
+constexpr int kDMaxSplit = 4;      // consumer warps sharing one step (each a part of I)
 constexpr int kDProducers = 2;     // producer warps (alternate stages)
 constexpr int kDRows = 16;         // output dims per CTA
 constexpr int kDMaxPairs = 8;      // (token, slot) pairs per step: one 8-column MMA tile
@@ -83,28 +84,71 @@ constexpr int kDMaxSteps = kStreamMaxSlots;  // every step holds at least one pa
 __host__ __device__ constexpr int d_round(int v, int a) { return (v + a - 1) / a * a; }
 
 // Stage: [0, 16 I) the 16 down rows as [I/128][16][128] swizzled bytes;
-// [16 I, 16 I + 16 I/32) their scale codes [16][I/32]; from `hoff` the pairs'
-// FP16 h rows (up to P of them), `hpitch` apart.  Before the ring: the barriers, the E8M0 decode
-// table (256 FP32), the step list (int4 per step: first down row, first pair
-// in the slot lists, pairs) and the per-slot results [B*K][16] FP32.
+// [16 I, 16 I + 16 I/32) their scale codes [16][I/32].  Before the ring: the
+// barriers, the E8M0 decode table (256 FP32), the step list (int4 per step:
+// first down row, first pair in the slot lists, pairs) and the per-slot
+// results [G][B*K][16] FP32 (one table per part of I when G warps share a
+// step).
 struct DimLayout {
-  int hoff, hpitch, stage, bars, dec, steps, res, ring, total;
+  int stage, bars, dec, steps, res, ring, total;
 };
 
-__host__ __device__ inline DimLayout dim_layout(int I, int S, int P) {
+__host__ __device__ inline DimLayout dim_layout(int I, int S, int G) {
   DimLayout L;
-  L.hoff = d_round(kDRows * I + kDRows * (I / 32), 16);
-  // FP16 row rounded up to 128 bytes, plus 64: the two pair rows read by one
-  // quarter-warp fall in different halves of the 32 banks
-  L.hpitch = d_round(2 * I, 128) + 64;
-  L.stage = d_round(L.hoff + P * L.hpitch, 1024);
+  L.stage = d_round(kDRows * I + kDRows * (I / 32), 1024);
   L.bars = kXOffset;  // full, empty [kDMaxStages] (8 bytes each)
   L.dec = L.bars + 16 * kDMaxStages;
   L.steps = L.dec + 256 * 4;
   L.res = L.steps + kDMaxSteps * 16;
-  L.ring = d_round(L.res + kStreamMaxSlots * kDRows * 4, 1024);
+  L.ring = d_round(L.res + G * kStreamMaxSlots * kDRows * 4, 1024);
   L.total = L.ring + S * L.stage;
   return L;
+}
+
+// 16 bytes of data written by an earlier kernel and not written during this
+// one, through the read-only path.
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// Shared-memory loads the compiler may schedule freely (plain asm, no memory
+// clobber): a stage's reads carry the token of the mbarrier wait that made it
+// visible (so they cannot move above it) and the stage's release takes the
+// sums computed from them as inputs (so they cannot move below it).
+__device__ __forceinline__ uint32_t ld_s8(uint32_t a) {
+  uint16_t v;
+  asm("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ld_sf(uint32_t a) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_s64(uint32_t a) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// Bounded wait for a phase (as mbar_wait); returns 0 as a token to add to the
+// addresses of the data the phase guards, or 1 if the wait ran out.
+__device__ __forceinline__ uint32_t mbar_wait_token(uint32_t bar, uint32_t parity, bool& ok) {
+  ok = mbar_wait(bar, parity);
+  uint32_t t;
+  asm volatile("mov.u32 %0, 0;" : "=r"(t) : "r"(ok ? 1u : 0u) : "memory");
+  return t;
+}
+
+// Arrive on `bar` once the eight sums (which depend on every read of the
+// stage) exist.
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, const float (&a)[2][4]) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar), "f"(a[0][0]), "f"(a[0][1]),
+               "f"(a[0][2]), "f"(a[0][3]), "f"(a[1][0]), "f"(a[1][1]), "f"(a[1][2]), "f"(a[1][3])
+               : "memory");
 }
 
 }  // namespace
@@ -169,20 +213,24 @@ __global__ void __launch_bounds__(64) moe_h_encode(const __nv_bfloat16* __restri
   if (lane == 0) hk[r] = k;
 }
 
-// Threads: NW consumer warps (each owning S / NW stages), then kDProducers
-// producer warps.  P: pairs per step (<= 8).
-// `tmap`: the down codes as a 3-D byte tensor {128, E * H, I / 128} with
-// strides {I, 128}, boxes {128, 16, I / 128}, 128-byte swizzle.  h16 / hk:
-// moe_h_encode's output for the B * K rows of h.
+// Threads: NW = NS x G consumer warps, then kDProducers producer warps.  The
+// consumers form NS step groups of G warps; group q takes the steps q, q + NS,
+// ... and owns the S / NS stages they use; within a group, warp part h does
+// the NB 32-column blocks [h NB, (h + 1) NB) of every step (NB x G = I / 32).
+// P: pairs per step (<= 8).  `tmap`: the down codes as a 3-D byte tensor
+// {128, E * H, I / 128} with strides {I, 128}, boxes {128, 16, I / 128},
+// 128-byte swizzle.  h16 / hk: moe_h_encode's output for the B * K rows of h.
+template <int NB>
 __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_dimblock(
     const __grid_constant__ CUtensorMap tmap, const __half* __restrict__ h16,
     const int32_t* __restrict__ hk, const int32_t* __restrict__ topk_ids,
     const float* __restrict__ topk_w, const uint8_t* __restrict__ down_scale,
     __nv_bfloat16* __restrict__ out, uint32_t* __restrict__ error_flag, int B, int H, int I,
-    int E, int K, int S, int NW, int P) {
+    int E, int K, int S, int NS, int G, int P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const RoutingTables rt = routing_tables_at(smem);
-  const DimLayout L = dim_layout(I, S, P);
+  const DimLayout L = dim_layout(I, S, G);
+  const int NW = NS * G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BK = B * K, nblk = I >> 5;
   const int d0 = blockIdx.x * kDRows;
@@ -193,7 +241,7 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full + 8 * s, 1);   // the producer's arrive (with the step's bytes)
-      mbar_init(empty + 8 * s, 1);  // the stage's consumer warp
+      mbar_init(empty + 8 * s, G);  // the stage's consumer warps
     }
     mbar_init_fence();
   }
@@ -218,112 +266,104 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
   auto step_at = [&](int i) -> int { const int t = i + rot; return t < nsteps ? t : t - nsteps; };
 
   if (warp >= NW) {  // producers: warp NW + p issues the steps whose stage s has s % 2 == p
-    if (nsteps == 0) return;
+    if (nsteps == 0 || lane != 0) return;
     const int p = warp - NW;
     auto mine = [&](int i) { return (i % S) % kDProducers == p; };
     const uint32_t wbytes = (uint32_t)(kDRows * I + kDRows * nblk);
-    const uint8_t* hg = nullptr;
-    // lane 0: the stage's byte count, the 16 rows and their scale codes
-    auto issue_weights = [&](uint32_t s, const int4& st_info) {
+    // the stage's byte count, the 16 rows and their scale codes (the weights
+    // do not depend on the kernel before this one)
+    auto issue = [&](uint32_t s, const int4& st_info) {
       const uint32_t st = ring + s * L.stage;
-      mbar_arrive_expect_tx(full + 8 * s, wbytes + (uint32_t)(st_info.z * 2 * I));
+      mbar_arrive_expect_tx(full + 8 * s, wbytes);
       tma_load_3d(st, &tmap, 0, st_info.x, 0, full + 8 * s);  // row < 2^31 (checked on launch)
       bulk_g2s_nohint(st + kDRows * I, down_scale + (size_t)st_info.x * nblk,
                       (uint32_t)(kDRows * nblk), full + 8 * s);
     };
-    // lane t < pairs: pair t's FP16 h row
-    auto issue_h = [&](uint32_t s, const int4& st_info) {
-      if (lane < st_info.z)
-        bulk_g2s_nohint(ring + s * L.stage + L.hoff + lane * L.hpitch,
-                        hg + (size_t)rt.slots[st_info.y + lane] * I * 2, (uint32_t)(2 * I),
-                        full + 8 * s);
-    };
-    const int npre = min(S, nsteps);
-    // the first S steps' weights go out before waiting for the grid that writes h16
-    if (lane == 0)
-      for (int i = 0; i < npre; ++i)
-        if (mine(i)) issue_weights(i, step_tab[step_at(i)]);
-    hg = reinterpret_cast<const uint8_t*>(h16) + grid_dependency_wait();
-    __syncwarp();
-    for (int i = 0; i < npre; ++i)
-      if (mine(i)) issue_h(i, step_tab[step_at(i)]);
-    int i = npre;
+    int i = 0;
     for (; i < nsteps; ++i) {
       if (!mine(i)) continue;
-      const uint32_t s = i % S, r = i / S;  // r >= 1 here
-      const int4 st_info = step_tab[step_at(i)];
-      bool free = true;
-      if (lane == 0) free = mbar_wait(empty + 8 * s, (r - 1) & 1);
-      if (!__shfl_sync(0xFFFFFFFFu, free ? 1 : 0, 0)) {
-        if (lane == 0 && error_flag) atomicOr(error_flag, 2u);
+      const uint32_t s = i % S;
+      if (i >= S && !mbar_wait(empty + 8 * s, ((i / S) - 1) & 1)) {
+        if (error_flag) atomicOr(error_flag, 2u);
         break;
       }
-      if (lane == 0) issue_weights(s, st_info);
-      __syncwarp();
-      issue_h(s, st_info);
+      issue(s, step_tab[step_at(i)]);
     }
-    if (lane == 0)  // the copies this warp issued last land before the CTA exits
-      for (int k = i - S > 0 ? i - S : 0; k < i && k < nsteps; ++k)
-        if (mine(k)) (void)mbar_wait(full + 8 * (k % S), (k / S) & 1);
+    // the copies this warp issued last land before the CTA exits
+    for (int k = i - S > 0 ? i - S : 0; k < i && k < nsteps; ++k)
+      if (mine(k)) (void)mbar_wait(full + 8 * (k % S), (k / S) & 1);
     return;
   }
 
-  // consumers: the routing weights and exponents are read at the end, after
-  // the wait for the kernel that writes the exponents (which also orders the
-  // writes of `out` after it)
+  // consumers: h16 and the exponents come from the kernel before this one,
+  // and the writes of `out` below must follow it too
   const uint32_t wait_token = grid_dependency_wait();
+  const uint8_t* hg = reinterpret_cast<const uint8_t*>(h16) + wait_token;
   const int g = lane >> 2, tig = lane & 3;
   const int pg = slab_row(g);  // the output dim (of 16) of tile rows g and g + 8
-  const float* dtab = reinterpret_cast<const float*>(smem + L.dec);
-  float* res = reinterpret_cast<float*>(smem + L.res);
+  const int grp = warp % NS, part = warp / NS;
+  const int j0 = part * NB;  // this warp's first block
+  const uint32_t dtab = base + L.dec;
+  float* res = reinterpret_cast<float*>(smem + L.res) + part * BK * kDRows;
   // this lane's A fragment offsets within a 4-block (128-column) slab, for
-  // row pg (row pg + 8 is 1024 bytes further); B and scale offsets at block 0
+  // row pg (row pg + 8 is 1024 bytes further), and its scale code offsets
   uint32_t a_off[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
     a_off[u] = (uint32_t)(pg * 128 + ((((u * 2 + (tig >> 1)) ^ (pg & 7))) << 4) + (tig & 1) * 8);
-  // B fragment rows: pair g; the tile's columns P..7 hold no pair and are
-  // never stored, so their lanes read the last pair row (inside the stage)
-  const uint32_t b_off = (uint32_t)(L.hoff + min(g, P - 1) * L.hpitch + tig * 16);
-  const uint32_t s_off = (uint32_t)(kDRows * I + pg * nblk);
+  const uint32_t a_base = (uint32_t)(j0 * 512);  // slab of the first block
+  const uint32_t s_off = (uint32_t)(kDRows * I + pg * nblk + j0);
   bool dead = false;
-  for (int i = warp; i < nsteps; i += NW) {
+  for (int i = grp; i < nsteps; i += NS) {
+    const int4 st_info = step_tab[step_at(i)];
+    // B fragments: this lane's columns of pair g's FP16 h row, 8 values (16
+    // bytes) per block, straight from global memory (written by the kernel
+    // before this one, resident in L2); requested before waiting for the
+    // weights so that both latencies overlap.  Columns >= pairs stay zero.
+    uint4 bf[NB];
+    const int slot_g = g < st_info.z ? rt.slots[st_info.y + g] : -1;
+    if (slot_g >= 0) {
+      const uint8_t* hrow = hg + (size_t)slot_g * I * 2 + (size_t)(j0 * 64 + tig * 16);
+#pragma unroll
+      for (int m = 0; m < NB; ++m) bf[m] = ld_global_nc_v4(hrow + m * 64);
+    } else {
+#pragma unroll
+      for (int m = 0; m < NB; ++m) bf[m] = make_uint4(0u, 0u, 0u, 0u);
+    }
     const uint32_t s = i % S;
-    if (!mbar_wait(full + 8 * s, (i / S) & 1)) {
+    bool ok;
+    const uint32_t tok = mbar_wait_token(full + 8 * s, (i / S) & 1, ok);
+    if (!ok) {
       dead = true;
       break;
     }
-    const uint8_t* st = smem + L.ring + s * L.stage;
+    const uint32_t st = ring + s * L.stage + tok;
     // two accumulators (even and odd blocks) halve the scale-FMA chain
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int j4 = 0; j4 < nblk; j4 += 4) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j4 + u;
-        const float sc0 = dtab[st[s_off + j]];
-        const float sc1 = dtab[st[s_off + 8 * nblk + j]];
-        const uint32_t a0 = (uint32_t)(j4 * 512) + a_off[u];  // slab j4 / 4, 2048 bytes each
-        const uint2 w0 = *reinterpret_cast<const uint2*>(st + a0);
-        const uint2 w1 = *reinterpret_cast<const uint2*>(st + a0 + 1024);
-        const uint4 b = *reinterpret_cast<const uint4*>(st + b_off + j * 64);
-        // columns 8 tig + 0..3 (first k16 step) and 8 tig + 4..7 (second)
-        float cc[4];
-        mma_f16_zero(cc, e4m3x2_lo_to_f16x2(w0.x), e4m3x2_lo_to_f16x2(w1.x),
-                     e4m3x2_hi_to_f16x2(w0.x), e4m3x2_hi_to_f16x2(w1.x), b.x, b.y);
-        mma_f16_acc(cc, e4m3x2_lo_to_f16x2(w0.y), e4m3x2_lo_to_f16x2(w1.y),
-                    e4m3x2_hi_to_f16x2(w0.y), e4m3x2_hi_to_f16x2(w1.y), b.z, b.w);
-        float(&a)[4] = acc[u & 1];
-        a[0] = fmaf(cc[0], sc0, a[0]);
-        a[1] = fmaf(cc[1], sc0, a[1]);
-        a[2] = fmaf(cc[2], sc1, a[2]);
-        a[3] = fmaf(cc[3], sc1, a[3]);
-      }
+    for (int m = 0; m < NB; ++m) {
+      const float sc0 = ld_sf(dtab + 4 * ld_s8(st + s_off + m));
+      const float sc1 = ld_sf(dtab + 4 * ld_s8(st + s_off + 8 * nblk + m));
+      const uint32_t a0 = a_base + (uint32_t)((m & ~3) * 512) + a_off[m & 3];  // 2048-byte slabs
+      const uint2 w0 = ld_s64(st + a0);
+      const uint2 w1 = ld_s64(st + a0 + 1024);
+      const uint4 b = bf[m];
+      // columns 8 tig + 0..3 (first k16 step) and 8 tig + 4..7 (second)
+      float cc[4];
+      mma_f16_zero(cc, e4m3x2_lo_to_f16x2(w0.x), e4m3x2_lo_to_f16x2(w1.x),
+                   e4m3x2_hi_to_f16x2(w0.x), e4m3x2_hi_to_f16x2(w1.x), b.x, b.y);
+      mma_f16_acc(cc, e4m3x2_lo_to_f16x2(w0.y), e4m3x2_lo_to_f16x2(w1.y),
+                  e4m3x2_hi_to_f16x2(w0.y), e4m3x2_hi_to_f16x2(w1.y), b.z, b.w);
+      float(&a)[4] = acc[m & 1];
+      a[0] = fmaf(cc[0], sc0, a[0]);
+      a[1] = fmaf(cc[1], sc0, a[1]);
+      a[2] = fmaf(cc[2], sc1, a[2]);
+      a[3] = fmaf(cc[3], sc1, a[3]);
     }
     // every lane is done with the stage (the sums depend on all its reads)
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty + 8 * s);
-    // this lane's pair columns 2 tig, 2 tig + 1: final sums of those slots
-    const int4 st_info = step_tab[step_at(i)];
+    if (lane == 0) mbar_arrive_after(empty + 8 * s, acc);
+    // this lane's pair columns 2 tig, 2 tig + 1: its part's sums of those slots
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int pc = 2 * tig + q;
@@ -337,6 +377,7 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
   if (dead && lane == 0 && error_flag) atomicOr(error_flag, 2u);
   // all slots' results are in: y = sum over k of result * w * 2^-k, k in order
   named_barrier_sync(1, NW * 32);
+  res = reinterpret_cast<float*>(smem + L.res);
   for (int idx = tid; idx < kDRows * B; idx += NW * 32) {
     const int b = idx / kDRows, row = idx - b * kDRows;
     float y = 0.0f;
@@ -346,7 +387,9 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
       if (e < 0 || e >= E) continue;
       const int ke = __ldcg(hk + slot + wait_token);
       const float f1 = exp2_int(-(ke >> 1)), f2 = exp2_int(-(ke - (ke >> 1)));
-      y = fmaf((res[slot * kDRows + row] * f1) * f2, __ldg(topk_w + slot), y);
+      float r = res[slot * kDRows + row];
+      for (int h = 1; h < G; ++h) r += res[(h * BK + slot) * kDRows + row];
+      y = fmaf((r * f1) * f2, __ldg(topk_w + slot), y);
     }
     out[(size_t)b * H + d0 + row] = __float2bfloat16_rn(y);
   }
@@ -355,36 +398,50 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
 namespace {
 
 struct DimShape {
-  int NW, S, P;  // consumer warps, ring stages (NW x stages per warp), pairs per step
+  int NS, S, P, G;  // step groups, ring stages (NS x stages per group), pairs per step, warps per step
 };
 
-// The built-in shape for I: four consumer warps with two stages each and six
-// pairs per step (at I = 768), else the largest of those that fits.
-DimShape dim_shape(int I, int want_nw, int want_spw, int want_p) {
-  if (want_nw > 0 && want_spw > 0 && want_p > 0) {
-    const DimShape d{want_nw, want_nw * want_spw, want_p};
-    if (d.NW <= kDMaxWarps && d.S <= kDMaxStages && d.P <= kDMaxPairs &&
-        dim_layout(I, d.S, d.P).total <= kDSmemCap)
-      return d;
+bool dim_fits(int I, const DimShape& d) {
+  const int nblk = I / 32;
+  const int nb = d.G > 0 ? nblk / d.G : 0;
+  return d.NS >= 1 && d.G >= 1 && d.G <= kDMaxSplit && d.NS * d.G <= kDMaxWarps && d.S >= d.NS &&
+         d.S % d.NS == 0 && d.S <= kDMaxStages && d.P >= 1 && d.P <= kDMaxPairs &&
+         nblk % d.G == 0 && (nb == 4 || nb == 8 || nb == 12 || nb == 16) &&
+         dim_layout(I, d.S, d.G).total <= kDSmemCap;
+}
+
+// The built-in shape for I: up to four step groups, each warp of a group
+// owning at most 16 blocks of 32 columns (two warps of 12 at I = 768), 8
+// pairs per step, and as many stages per group as fit (three at I = 768).
+DimShape dim_shape(int I, int want_ns, int want_spg, int want_p, int want_g) {
+  if (want_ns > 0 && want_spg > 0 && want_p > 0 && want_g > 0) {
+    const DimShape d{want_ns, want_ns * want_spg, want_p, want_g};
+    if (dim_fits(I, d)) return d;
   }
-  for (int nw = 4; nw >= 1; --nw)
-    if (dim_layout(I, 2 * nw, 6).total <= kDSmemCap) return DimShape{nw, 2 * nw, 6};
-  return DimShape{0, 0, 0};
+  for (int g = 1; g <= kDMaxSplit; g *= 2)
+    for (int ns = 4; ns >= 1; --ns)
+      for (int spg = kDMaxStages / ns; spg >= 2; --spg) {
+        const DimShape d{ns, ns * spg, kDMaxPairs, g};
+        if (dim_fits(I, d) && d.NS * d.G <= kDMaxWarps) return d;
+      }
+  return DimShape{0, 0, 0, 0};
 }
 
 }  // namespace
 
-int down_dimblock_shape(int I, int want_nw, int want_spw, int want_p, int* S, int* P) {
-  const DimShape d = dim_shape(I, want_nw, want_spw, want_p);
+int down_dimblock_shape(int I, int want_ns, int want_spg, int want_p, int want_g, int* S, int* P,
+                        int* G) {
+  const DimShape d = dim_shape(I, want_ns, want_spg, want_p, want_g);
   *S = d.S;
   *P = d.P;
-  return d.NW;
+  *G = d.G;
+  return d.NS;
 }
 
 bool down_dimblock_supported(int B, int H, int I, int E, int K) {
   return B <= kDMaxB && B * K <= kStreamMaxSlots && E <= 4096 && H % kDRows == 0 &&
          I % 128 == 0 && I <= 4096 && (long long)E * H < (1ll << 31) &&
-         dim_shape(I, 0, 0, 0).NW >= 1;
+         dim_shape(I, 0, 0, 0, 0).NS >= 1;
 }
 
 cudaError_t launch_h_encode(const void* h, void* h16, int32_t* hk, int rows, int I,
@@ -402,25 +459,21 @@ cudaError_t launch_h_encode(const void* h, void* h16, int32_t* hk, int rows, int
                             reinterpret_cast<__half*>(h16), hk, rows, I);
 }
 
-// p.rpw: consumer warps, p.qpl: ring stages, p.pairs: pairs per step (all
-// resolved by the plan).  a.h is unused: the operands are `h16` and `hk`
-// (moe_h_encode's output for a.h).
-cudaError_t launch_down_dimblock(const DownArgs& a, const DownPlan& p, const void* h16,
-                                 const int32_t* hk, cudaStream_t stream, bool pdl) {
-  if (!down_dimblock_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
-  int S = 0, P = 0;
-  const int NW = down_dimblock_shape(a.I, p.rpw, p.rpw > 0 ? p.qpl / p.rpw : 0, p.pairs, &S, &P);
-  if (NW < 1 || S % NW != 0) return cudaErrorInvalidValue;
-  const int smem = dim_layout(a.I, S, P).total;
+template <int NB>
+static cudaError_t launch_dimblock_t(const DownArgs& a, int S, int NS, int G, int P,
+                                     const void* h16, const int32_t* hk, cudaStream_t stream,
+                                     bool pdl) {
+  const int smem = dim_layout(a.I, S, G).total;
   {
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(moe_down_dimblock), smem);
+    const cudaError_t e =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(moe_down_dimblock<NB>), smem);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap map;
   if (!encode_row_slab_map(&map, a.down, (uint64_t)a.E * a.H, a.I)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.H / kDRows));
-  cfg.blockDim = dim3(32 * (NW + kDProducers));
+  cfg.blockDim = dim3(32 * (NS * G + kDProducers));
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -428,10 +481,29 @@ cudaError_t launch_down_dimblock(const DownArgs& a, const DownPlan& p, const voi
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, moe_down_dimblock, map, reinterpret_cast<const __half*>(h16), hk,
-                            a.topk_ids, a.topk_w, a.down_scale,
+  return cudaLaunchKernelEx(&cfg, moe_down_dimblock<NB>, map, reinterpret_cast<const __half*>(h16),
+                            hk, a.topk_ids, a.topk_w, a.down_scale,
                             reinterpret_cast<__nv_bfloat16*>(a.out), a.error_flag, a.B, a.H, a.I,
-                            a.E, a.K, S, NW, P);
+                            a.E, a.K, S, NS, G, P);
+}
+
+// p.rpw: step groups, p.qpl: ring stages, p.pairs: pairs per step, p.split:
+// warps per step (all resolved by the plan).  a.h is unused: the operands are
+// `h16` and `hk` (moe_h_encode's output for a.h).
+cudaError_t launch_down_dimblock(const DownArgs& a, const DownPlan& p, const void* h16,
+                                 const int32_t* hk, cudaStream_t stream, bool pdl) {
+  if (!down_dimblock_supported(a.B, a.H, a.I, a.E, a.K)) return cudaErrorInvalidValue;
+  int S = 0, P = 0, G = 0;
+  const int NS = down_dimblock_shape(a.I, p.rpw, p.rpw > 0 ? p.qpl / p.rpw : 0, p.pairs, p.split,
+                                     &S, &P, &G);
+  if (NS < 1 || S % NS != 0) return cudaErrorInvalidValue;
+  switch (a.I / 32 / G) {
+    case 4: return launch_dimblock_t<4>(a, S, NS, G, P, h16, hk, stream, pdl);
+    case 8: return launch_dimblock_t<8>(a, S, NS, G, P, h16, hk, stream, pdl);
+    case 12: return launch_dimblock_t<12>(a, S, NS, G, P, h16, hk, stream, pdl);
+    case 16: return launch_dimblock_t<16>(a, S, NS, G, P, h16, hk, stream, pdl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace wd

@@ -54,10 +54,11 @@ enum DownVariant {
   kDownDimBlock = 1,  // moe_h_encode + moe_down_dimblock: CTA per 16 output dims, all experts
 };
 struct DownPlan {
-  int rpw;          // batched: output dims per warp; dimblock: consumer warps
+  int rpw;          // batched: output dims per warp; dimblock: step groups
   int qpl;          // batched: virtual blocks per lane per pass; dimblock: ring stages
   int variant = 0;  // DownVariant
   int pairs = 0;    // dimblock: (token, slot) pairs per step
+  int split = 0;    // dimblock: consumer warps per step
 };
 
 GateUpPlan plan_gate_up(int B, int H, int I, int K, int E);
@@ -101,10 +102,11 @@ cudaError_t launch_gate_up_mma(const GateUpArgs& a, const GateUpPlan& p, cudaStr
 bool gate_up_mma_supported(int B, int H, int I, int E, int K);
 cudaError_t launch_down(const DownArgs& a, const DownPlan& p, cudaStream_t stream, bool pdl);
 bool down_dimblock_supported(int B, int H, int I, int E, int K);
-// moe_down_dimblock's shape for I: consumer warps (returned), ring stages and
-// pairs per step; the wanted shape if all three are given and it fits, else
-// the built-in one; 0 warps if none fits.
-int down_dimblock_shape(int I, int want_nw, int want_spw, int want_p, int* S, int* P);
+// moe_down_dimblock's shape for I: step groups (returned), ring stages, pairs
+// per step and warps per step; the wanted shape if all four are given and it
+// fits, else the built-in one; 0 groups if none fits.
+int down_dimblock_shape(int I, int want_ns, int want_spg, int want_p, int want_g, int* S, int* P,
+                        int* G);
 cudaError_t launch_h_encode(const void* h, void* h16, int32_t* hk, int rows, int I,
                             cudaStream_t stream, bool pdl);
 cudaError_t launch_down_dimblock(const DownArgs& a, const DownPlan& p, const void* h16,

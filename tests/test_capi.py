@@ -165,10 +165,10 @@ def test_built_in_plan_by_batch():
         "gate_up=moe_gate_up_mma<8,0> down=moe_down_3d_batched<4,1> pdl=1 launches=2"
     for B in (16, 32):
         assert wd.wd_moe_describe_plan(B, **q) == \
-            "gate_up=moe_gate_up_mma<8,0> down=moe_down_dimblock<4,2,6> pdl=7 launches=3"
+            "gate_up=moe_gate_up_mma<8,0> down=moe_down_dimblock<4,3,8,2> pdl=7 launches=3"
     # H above the tensor-core gate/up kernel's limit: the CUDA-core persistent kernel
     assert wd.wd_moe_describe_plan(32, 4096, 768, 128, 8).startswith(
-        "gate_up=moe_gate_up_persist<2,1> down=moe_down_dimblock<4,2,6>")
+        "gate_up=moe_gate_up_persist<2,1> down=moe_down_dimblock<4,3,8,2>")
     # B*K above the persistent kernels' routing tables: shared-row gate/up, batched down
     assert wd.wd_moe_describe_plan(64, **q) == \
         "gate_up=moe_gate_up_rowshare<2,2> down=moe_down_3d_batched<4,1> pdl=3 launches=2"
@@ -181,9 +181,9 @@ def test_built_in_plan_by_batch():
     finally:
         wd.wd_moe_set_plan(None)
     # the shared-row down on request even where tokens rarely share experts
-    wd.wd_moe_set_plan("dn=dimblock:3:3:5")
+    wd.wd_moe_set_plan("dn=dimblock:1:3:3:2")
     try:
-        assert wd.wd_moe_describe_plan(2, **q).endswith("down=moe_down_dimblock<3,3,5> pdl=7 launches=3")
+        assert wd.wd_moe_describe_plan(2, **q).endswith("down=moe_down_dimblock<1,3,3,2> pdl=7 launches=3")
         assert "down=moe_down_3d_batched<4,1>" in wd.wd_moe_describe_plan(128, 2048, 768, 128, 2)
     finally:
         wd.wd_moe_set_plan(None)
@@ -202,9 +202,9 @@ def test_plan_override_parser():
     assert lib.wd_moe_set_plan(b"gu=mma,pdl=3") == OK
     assert lib.wd_moe_set_plan(b"gu=mma:2,pdl=0") == OK
     assert lib.wd_moe_set_plan(b"gu=mma:2:16,dn=dimblock") == OK
-    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6,pdl=7") == OK
-    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2") == INVALID
-    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6:1") == INVALID
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6:2,pdl=7") == OK
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6") == INVALID
+    assert lib.wd_moe_set_plan(b"dn=dimblock:4:2:6:1:1") == INVALID
     # kernels that are no longer part of the library
     for gone in (b"gu=tma", b"gu=ring:2", b"dn=emma", b"dn=shared:2", b"dn=persist:4:1"):
         assert lib.wd_moe_set_plan(gone) == INVALID

@@ -237,9 +237,9 @@ PLANS = [
     "gu=mma,dn=4:1",
     "gu=mma:2:16,dn=4:1",
     "gu=mma,dn=dimblock",
-    "gu=mma,dn=dimblock:2:1:3",
-    "gu=mma,dn=dimblock:5:2:4",
-    "gu=mma,dn=dimblock:1:1:1",
+    "gu=mma,dn=dimblock:2:1:3:2",
+    "gu=mma,dn=dimblock:4:3:1:2",
+    "gu=mma,dn=dimblock:1:2:8:1",
     "gu=batched:2:1,dn=dimblock,pdl=0",
 ]
 
@@ -388,8 +388,10 @@ def test_gate_up_mma_special_scale_codes(cuda_device, plan_reset):
 # 2 per expert), two CTAs (H = 32) and six (H = 96), I = 128 (four blocks per
 # step), I = 2048 (a two-stage ring, one consumer warp), ~13 pairs per expert
 # (a third, partly empty step), duplicate-prone K == E, and a single token;
-# each with the built-in shape (4 consumer warps, 2 stages each, 6 pairs per
-# step) and with 1 warp x 2 stages x 6 pairs, 2 x 2 x 8 and 3 x 3 x 5.
+# each with the built-in shape (at I = 768: 4 step groups of 2 warps, 3 stages
+# per group, 8 pairs per step) and with (groups, stages per group, pairs,
+# warps per step) = (2, 2, 8, 2), (1, 3, 3, 2) and (4, 2, 5, 1) where they fit
+# (the built-in shape where they do not).
 DN_SHAPES = [
     (8, 2048, 768, 128, 8, "uniform"),
     (16, 2048, 768, 128, 8, "uniform"),
@@ -407,8 +409,8 @@ DN_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("plan", ["dn=dimblock", "dn=dimblock:1:2:6", "dn=dimblock:2:2:8",
-                                  "dn=dimblock:3:3:5"])
+@pytest.mark.parametrize("plan", ["dn=dimblock", "dn=dimblock:2:2:8:2", "dn=dimblock:1:3:3:2",
+                                  "dn=dimblock:4:2:5:1"])
 @pytest.mark.parametrize("B,H,I,E,K,route", DN_SHAPES)
 def test_down_dimblock_matches_the_oracle(cuda_device, plan_reset, B, H, I, E, K, route, plan):
     wd.wd_moe_set_plan(plan)
