@@ -306,7 +306,10 @@ def time_graph(torch, dev, g, s, steps, warmup, barrier):
 def time_kernels_alone(torch, wd, dev, stack, buf, steps):
     """Per-launch device time of each kernel of the plan on its own (no
     overlap), CUDA events on the launching stream around every launch; weights
-    are cold (48 layers between two uses).  Returns {kernel: {...}}."""
+    are cold (48 layers between two uses).  Each step is queued behind a hold
+    kernel, so the device runs the whole queued step back to back and the
+    events measure kernels, not the host's launch rate (a B=1 kernel is
+    shorter than one Python launch call).  Returns {kernel: {...}}."""
     B, K, I, H, E = buf["B"], stack.K, stack.I, stack.H, stack.E
     plan = plan_of(wd, B, H, I, E, K)
     shared_down = plan["down"].startswith("moe_down_dimblock")
@@ -323,6 +326,7 @@ def time_kernels_alone(torch, wd, dev, stack, buf, steps):
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(s):
         for _ in range(steps):
+            wd.wd_bench_hold(40000, stream=s)
             for l in range(stack.L):
                 gu, gus, dn, dns = stack.weights[l]
                 ids, w = buf["ids"][l], buf["w"][l]

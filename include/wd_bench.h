@@ -10,7 +10,11 @@
  *                    (read + write), the copy-kernel convention;
  *   wd_bench_read  - streams src once (read only) and folds it into *sink;
  *   wd_bench_fill  - writes a pattern over buf (used to evict L2 between timed
- *                    runs when buf is larger than L2).
+ *                    runs when buf is larger than L2);
+ *   wd_bench_hold  - occupies `stream` for a while with one thread, so that the
+ *                    host can queue a long run of short launches behind it and
+ *                    time each one on the device without the gaps of the
+ *                    host's own launch rate.
  * All pointers are device pointers owned by the caller; src/dst/buf must be
  * 32-byte aligned and `bytes` a multiple of 32.  `blocks` is the grid size
  * (0: 8 CTAs of 256 threads per SM).  Asynchronous on `stream`; returns 0 on
@@ -33,6 +37,11 @@ extern "C" {
 WD_API int wd_bench_copy(void* dst, const void* src, size_t bytes, int blocks, void* stream);
 WD_API int wd_bench_read(const void* src, size_t bytes, uint32_t* sink, int blocks, void* stream);
 WD_API int wd_bench_fill(void* buf, size_t bytes, uint32_t value, int blocks, void* stream);
+
+/* One single-thread kernel on `stream` that returns after `microseconds`
+ * (at most 1,000,000; larger values return cudaErrorInvalidValue) of the
+ * device's global timer have passed.  0 on success, else the launch's error. */
+WD_API int wd_bench_hold(unsigned int microseconds, void* stream);
 
 /* Number of streaming multiprocessors of the current device (or -1). */
 WD_API int wd_bench_sm_count(void);

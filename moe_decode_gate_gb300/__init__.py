@@ -23,6 +23,7 @@ from ._native import (  # noqa: F401
     lib,
     wd_bench_copy,
     wd_bench_fill,
+    wd_bench_hold,
     wd_bench_read,
     wd_bench_sm_count,
     wd_bench_spec_gbs,

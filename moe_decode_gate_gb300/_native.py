@@ -47,6 +47,7 @@ SIGNATURES = {
     "wd_bench_copy": (_I, [_P, _P, _SZ, _I, _P]),
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
+    "wd_bench_hold": (_I, [_U32, _P]),
     "wd_bench_sm_count": (_I, []),
     "wd_bench_spec_gbs": (ctypes.c_double, []),
 }
@@ -260,6 +261,11 @@ def wd_bench_read(src, sink, nbytes=None, blocks=0, stream=None):
 def wd_bench_fill(buf, value=0, nbytes=None, blocks=0, stream=None):
     n = nbytes if nbytes is not None else buf.numel() * buf.element_size()
     _check("wd_bench_fill", lib().wd_bench_fill(_ptr(buf), n, value, blocks, _stream(stream)))
+
+
+def wd_bench_hold(microseconds, stream=None):
+    """Occupy `stream` for `microseconds` of device time (one thread)."""
+    _check("wd_bench_hold", lib().wd_bench_hold(int(microseconds), _stream(stream)))
 
 
 def wd_bench_sm_count() -> int:

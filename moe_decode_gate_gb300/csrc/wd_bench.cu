@@ -84,6 +84,18 @@ __global__ void __launch_bounds__(256) fill_kernel(uint8_t* __restrict__ buf, si
                  : "memory");
 }
 
+// One thread that returns once `ns` nanoseconds of %globaltimer have passed
+// (or after a fixed number of polls, whichever comes first).
+__global__ void hold_kernel(unsigned long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (int i = 0; i < (1 << 22); ++i) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 >= ns) break;
+    __nanosleep(1000);
+  }
+}
+
 bool ok32(const void* p, size_t bytes) {
   return p && (reinterpret_cast<uintptr_t>(p) % 32) == 0 && bytes % 32 == 0;
 }
@@ -131,6 +143,12 @@ int wd_bench_fill(void* buf, size_t bytes, uint32_t value, int blocks, void* str
   if (!ok32(buf, bytes)) return (int)cudaErrorInvalidValue;
   fill_kernel<<<blocks_or_default(blocks), 256, 0, (cudaStream_t)stream>>>((uint8_t*)buf,
                                                                           bytes / 32, value);
+  return (int)cudaGetLastError();
+}
+
+int wd_bench_hold(unsigned int microseconds, void* stream) {
+  if (microseconds > 1000000u) return (int)cudaErrorInvalidValue;
+  hold_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(1000ull * microseconds);
   return (int)cudaGetLastError();
 }
 

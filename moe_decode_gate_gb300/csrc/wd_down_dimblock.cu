@@ -134,15 +134,6 @@ __device__ __forceinline__ uint2 ld_s64(uint32_t a) {
   return v;
 }
 
-// Bounded wait for a phase (as mbar_wait); returns 0 as a token to add to the
-// addresses of the data the phase guards, or 1 if the wait ran out.
-__device__ __forceinline__ uint32_t mbar_wait_token(uint32_t bar, uint32_t parity, bool& ok) {
-  ok = mbar_wait(bar, parity);
-  uint32_t t;
-  asm volatile("mov.u32 %0, 0;" : "=r"(t) : "r"(ok ? 1u : 0u) : "memory");
-  return t;
-}
-
 // Arrive on `bar` once the eight sums (which depend on every read of the
 // stage) exist.
 __device__ __forceinline__ void mbar_arrive_after(uint32_t bar, const float (&a)[2][4]) {

@@ -1,6 +1,6 @@
 // wd_mma.cuh - pieces shared by the tensor-core kernels (moe_gate_up_mma,
-// moe_down_mma): E4M3 -> FP16 conversion into MMA fragments, the warp-level
-// m16n8k16 MMA, 3-D tensor-map and bulk copies into shared memory, the
+// moe_down_dimblock): E4M3 -> FP16 conversion into MMA fragments, the
+// warp-level m16n8k16 MMA, 3-D tensor-map copies into shared memory, the
 // swizzled layout those copies produce, FP16 re-encoding of BF16 activations
 // by a power of two, and the host-side tensor-map encoder.
 #pragma once
@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+
+#include "wd_pipeline.cuh"
 
 namespace wd {
 
@@ -34,16 +36,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-
-// Bulk copy global -> shared without an L2 cache hint.
-__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
-                                                uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

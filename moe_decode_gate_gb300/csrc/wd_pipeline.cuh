@@ -75,6 +75,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Bulk copy global -> shared without an L2 cache hint.
+__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Bounded wait for a phase (as mbar_wait); returns 0 as a token to add to the
+// shared-memory addresses of the data the phase guards (so that plain-asm
+// reads of them cannot be scheduled above the wait); `ok` is false if the wait
+// ran out.
+__device__ __forceinline__ uint32_t mbar_wait_token(uint32_t bar, uint32_t parity, bool& ok) {
+  ok = mbar_wait(bar, parity);
+  uint32_t t;
+  asm volatile("mov.u32 %0, 0;" : "=r"(t) : "r"(ok ? 1u : 0u) : "memory");
+  return t;
+}
+
 // L2 policy for data read exactly once per launch (weight rows): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;

@@ -32,7 +32,7 @@ def test_headers_declare_the_expected_entry_points():
     for n in ("wd_moe_decode", "wd_moe_gate_up", "wd_moe_down", "wd_moe_down_workspace",
               "wd_moe_workspace_size", "wd_moe_workspace_init", "wd_moe_read_error_flag",
               "wd_status_string", "wd_moe_launches", "wd_bench_copy", "wd_bench_read",
-              "wd_bench_fill"):
+              "wd_bench_fill", "wd_bench_hold"):
         assert n in names
 
 
@@ -135,6 +135,7 @@ def test_bench_kernels_reject_unaligned_buffers():
     assert lib.wd_bench_copy(A32, A32, 1000, 0, None) == einval
     assert lib.wd_bench_read(A32, 1024, None, 0, None) == einval
     assert lib.wd_bench_fill(None, 1024, 0, 0, None) == einval
+    assert lib.wd_bench_hold(1000001, None) == einval  # longer than a second
 
 
 def test_last_error_string_starts_empty():
