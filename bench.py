@@ -24,6 +24,10 @@ The headline line is B=32; alongside it:
     stack's activations collapse to zero after a few layers);
   - each kernel of the plan timed alone, and the roofline of the one that
     takes longest per launch;
+  - the expert-centric comparison layer (padding, gather, grouped GEMVs,
+    per-expert output buffer, combine) on the same stack at every B of the
+    sweep and at B = 64, 128, 256 (the crossover beyond decode), with
+    vs_expert_centric = its time / this library's time;
   - the same step end to end through the public API with host buffers;
   - the FP64 CPU oracle on one host core and on all of them.
 
@@ -60,6 +64,8 @@ COMPARE_PLANS = {
     "per_token_down": "gu=mma,dn=4:1,pdl=1",  # shared-row gate/up, per-(token, dims) down
 }
 L2_FLUSH_BYTES = 512 << 20  # written before every cold single-layer call (L2 is 126 MB)
+# batches beyond decode where the expert-centric path is timed against this one
+CROSSOVER_B = (64, 128, 256)
 
 
 # ------------------------------------------------------------------ helpers --
@@ -101,11 +107,13 @@ def read_peaks_file():
 
 
 def kernel_sources_sha():
-    """sha256 prefix of the device-code sources (the C-ABI's host code and the
-    bench's own copy/read kernels are left out)."""
+    """sha256 prefix of the layer's device-code sources (the C-ABI's host code,
+    the bench's copy/read kernels and the expert-centric comparison layer are
+    left out)."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(os.path.join(ROOT, "moe_decode_gate_gb300", "csrc"))):
-        if not f.endswith((".cu", ".cuh", ".h")) or f in ("wd_capi.cu", "wd_bench.cu"):
+        if not f.endswith((".cu", ".cuh", ".h")) or f in ("wd_capi.cu", "wd_bench.cu",
+                                                          "wd_expert_centric.cu"):
             continue
         with open(os.path.join(ROOT, "moe_decode_gate_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
@@ -260,26 +268,35 @@ class Stack:
         x = buf["x0"] if l == 0 else buf["act"][(l - 1) % 2]
         return x, buf["act"][l % 2]
 
-    def enqueue_step(self, buf, stream=None):
+    def enqueue_step(self, buf, stream=None, expert_centric=False):
+        """One step: every layer through wd_moe_decode, or (expert_centric) through
+        the expert-centric comparison layer with its own workspace."""
         wd = self.wd
         for l in range(self.L):
             gu, gus, dn, dns = self.weights[l]
             x, out = self.layer_io(buf, l)
-            wd.wd_moe_decode(x, buf["ids"][l], buf["w"][l], gu, gus, dn, dns, out, self.workspace,
-                             stream=stream)
+            if expert_centric:
+                wd.wd_bench_expert_centric(x, buf["ids"][l], buf["w"][l], gu, gus, dn, dns, out,
+                                           buf["ec_ws"], stream=stream)
+            else:
+                wd.wd_moe_decode(x, buf["ids"][l], buf["w"][l], gu, gus, dn, dns, out,
+                                 self.workspace, stream=stream)
         return buf["act"][(self.L - 1) % 2]
 
-    def graph(self, buf):
+    def graph(self, buf, expert_centric=False):
         torch = self.torch
+        if expert_centric and "ec_ws" not in buf:
+            n = self.wd.wd_bench_expert_centric_workspace_size(buf["B"], self.H, self.I, self.E, self.K)
+            buf["ec_ws"] = torch.empty(n, dtype=torch.uint8, device=self.dev)
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
-        with torch.cuda.stream(s):
-            self.enqueue_step(buf, stream=s)  # warm the launch path outside capture
+        with torch.cuda.stream(s):  # warm the launch path outside capture
+            self.enqueue_step(buf, stream=s, expert_centric=expert_centric)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            self.enqueue_step(buf, stream=s)
+            self.enqueue_step(buf, stream=s, expert_centric=expert_centric)
         return g, s
 
     def launches_per_step(self, B):
@@ -438,9 +455,12 @@ def time_single_layers(torch, wd, dev, peak, iters, log):
     captured once in a CUDA graph; before every timed replay the L2 is flushed
     by writing L2_FLUSH_BYTES (untimed, and long enough for the host to queue
     the events and the replay behind it, so no launch gap is timed); events on
-    the replaying stream around the replay; median over `iters` replays."""
+    the replaying stream around the replay; median over `iters` replays.  The
+    flush buffer is then read once (also untimed), so the L2 holds clean lines
+    and the timed call pays no write-back of the flush."""
     rows = []
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
     s = torch.cuda.Stream(device=dev)
     cases = [("qwen3_b1", (1,)), ("qwen3_sweep", SWEEP_B), ("qwen3_zipf", (32,)),
              ("qwen3_fixed", (32,)), ("qwen3_disjoint", (32,))]
@@ -470,6 +490,7 @@ def time_single_layers(torch, wd, dev, peak, iters, log):
             with torch.cuda.stream(s):
                 for it in range(iters + 2):
                     wd.wd_bench_fill(flush, 0x5A5A5A5A + it, stream=s)
+                    wd.wd_bench_read(flush, sink, stream=s)
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
                     a.record(s)
@@ -755,7 +776,8 @@ def main():
     log(f"peaks {peaks}, fraction denominator {peak_ref} GB/s")
 
     sweep = [int(b) for b in args.sweep.split(",") if b] if not args.quick else []
-    max_b = max([HEADLINE_B, args.batch] + sweep)
+    extras_on = not args.quick and not args.no_extras
+    max_b = max([HEADLINE_B, args.batch] + sweep + (list(CROSSOVER_B) if extras_on else []))
     stack = Stack(torch, wd, dev, args.layers, max_b, log)
     H, I, E, K = stack.H, stack.I, stack.E, stack.K
 
@@ -802,7 +824,40 @@ def main():
     log(f"roofline {roofline['kernel']}: {roofline['achieved']} GB/s = {roofline['frac']} of measured")
 
     extras = {}
-    if not args.quick and not args.no_extras:
+    if extras_on:
+        # ---- the expert-centric comparison path on the same stack, and the
+        # crossover beyond decode batches (both paths, B = 64..256) ----
+        ec_rows = []
+        wd_us = {r["B"]: r["us_per_layer"] for r in sweep_rows}
+        for Bx in sorted({r["B"] for r in sweep_rows} | set(CROSSOVER_B)):
+            bx = stack.buffers(Bx)
+            nbx = algorithmic_bytes(bx["ids_host"], Bx, H, I, E, K)
+            if Bx not in wd_us:
+                g, s = stack.graph(bx)
+                msx = max_over_ranks(time_graph(torch, dev, g, s, args.sweep_steps, 3, barrier))
+                del g
+                wd_us[Bx] = round(msx * 1e3 / stack.L, 2)
+            g, s = stack.graph(bx, expert_centric=True)
+            msx = max_over_ranks(time_graph(torch, dev, g, s, args.sweep_steps, 3, barrier))
+            del g
+            ec_us = round(msx * 1e3 / stack.L, 2)
+            ec_rows.append({"B": Bx, "expert_centric_us_per_layer": ec_us,
+                            "expert_centric_GBps": round(nbx / msx / 1e6, 1),
+                            "warp_decode_us_per_layer": wd_us[Bx],
+                            "vs_expert_centric": round(ec_us / wd_us[Bx], 3)})
+            log(f"expert-centric B={Bx}: {ec_rows[-1]}")
+        ratio = {r["B"]: r["vs_expert_centric"] for r in ec_rows}
+        for r in sweep_rows:
+            r["vs_expert_centric"] = ratio.get(r["B"])
+        extras["expert_centric"] = {
+            "what": "the same 48-layer stack through wd_bench_expert_centric (routing metadata, "
+                    "power-of-two padding, gather into expert-major buffers, grouped gate/up and "
+                    "down GEMVs into a per-expert BF16 output buffer, weighted combine: 5 launches "
+                    "per layer); vs_expert_centric = its time / this library's time (> 1: warp "
+                    "decode faster); B = 64..256 is the crossover beyond decode",
+            "rows": ec_rows}
+        extras["vs_expert_centric_b32"] = ratio.get(HEADLINE_B)
+    if extras_on:
         # ---- other plans on the same stack, B = 8..32 ----
         for name, spec in COMPARE_PLANS.items():
             wd.wd_moe_set_plan(spec)
@@ -842,7 +897,7 @@ def main():
                "how": "pinned H2D of x and all layers' ids/w, one wd_moe_decode call per layer "
                       "(no graph), D2H of out, events on the launching stream"}
 
-    if not args.quick and not args.no_extras:
+    if extras_on:
         del stack
         torch.cuda.empty_cache()
         extras["single_layers_cold"] = {

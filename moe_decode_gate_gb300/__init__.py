@@ -22,6 +22,8 @@ from ._native import (  # noqa: F401
     library_path,
     lib,
     wd_bench_copy,
+    wd_bench_expert_centric,
+    wd_bench_expert_centric_workspace_size,
     wd_bench_fill,
     wd_bench_hold,
     wd_bench_read,

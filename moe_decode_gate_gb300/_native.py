@@ -48,6 +48,9 @@ SIGNATURES = {
     "wd_bench_read": (_I, [_P, _SZ, _P, _I, _P]),
     "wd_bench_fill": (_I, [_P, _SZ, _U32, _I, _P]),
     "wd_bench_hold": (_I, [_U32, _P]),
+    "wd_bench_expert_centric_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "wd_bench_expert_centric": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I,
+                                     _P]),
     "wd_bench_sm_count": (_I, []),
     "wd_bench_spec_gbs": (ctypes.c_double, []),
 }
@@ -266,6 +269,22 @@ def wd_bench_fill(buf, value=0, nbytes=None, blocks=0, stream=None):
 def wd_bench_hold(microseconds, stream=None):
     """Occupy `stream` for `microseconds` of device time (one thread)."""
     _check("wd_bench_hold", lib().wd_bench_hold(int(microseconds), _stream(stream)))
+
+
+def wd_bench_expert_centric_workspace_size(B, H, I, E, K) -> int:
+    return int(lib().wd_bench_expert_centric_workspace_size(B, H, I, E, K))
+
+
+def wd_bench_expert_centric(x, topk_ids, topk_w, gate_up, gate_up_scale, down, down_scale, out,
+                            workspace, stream=None):
+    """The expert-centric comparison layer (include/wd_bench.h); shapes as wd_moe_decode."""
+    B, H = x.shape
+    E, two_i, _ = gate_up.shape
+    K = topk_ids.shape[1]
+    _check("wd_bench_expert_centric", lib().wd_bench_expert_centric(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_w), _ptr(gate_up), _ptr(gate_up_scale), _ptr(down),
+        _ptr(down_scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        B, H, two_i // 2, E, K, _stream(stream)))
 
 
 def wd_bench_sm_count() -> int:

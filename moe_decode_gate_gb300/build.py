@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libwd_moe.so")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["wd_gate_up.cu", "wd_gate_up_rowshare.cu", "wd_gate_up_persist.cu", "wd_gate_up_mma.cu",
-           "wd_down.cu", "wd_down_dimblock.cu", "wd_capi.cu", "wd_bench.cu", "wd_no_alloc.cu"]
+           "wd_down.cu", "wd_down_dimblock.cu", "wd_capi.cu", "wd_bench.cu", "wd_no_alloc.cu",
+           "wd_expert_centric.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-Xcompiler", "-Wall", "-I", os.path.join(ROOT, "include")]

@@ -138,6 +138,23 @@ def test_bench_kernels_reject_unaligned_buffers():
     assert lib.wd_bench_hold(1000001, None) == einval  # longer than a second
 
 
+def test_expert_centric_arguments_and_workspace():
+    lib = wd.lib()
+    size = wd.wd_bench_expert_centric_workspace_size
+    assert size(32, 2048, 768, 128, 8) > 2 * (2 * 32 * 8) * (2048 + 768 + 2048)  # three buffers
+    assert size(64, 2048, 768, 128, 8) > size(32, 2048, 768, 128, 8)
+    assert size(0, 2048, 768, 128, 8) == 0 and size(1, 2048, 768, 8192, 8) == 0
+    assert size(1, 8192, 768, 128, 8) == 0  # H above 4096
+    einval = 1
+    n = size(2, 256, 128, 8, 2)
+    assert lib.wd_bench_expert_centric(None, None, None, None, None, None, None, None, None, n,
+                                       2, 256, 128, 8, 2, None) == einval
+    assert lib.wd_bench_expert_centric(A32, A32, A32, A32, A32, A32, A32, A32, A32, n - 1,
+                                       2, 256, 128, 8, 2, None) == einval  # workspace too small
+    assert lib.wd_bench_expert_centric(A32, A32, A32, A32, A32, A32, A32, A32, A32 + 16, n,
+                                       2, 256, 128, 8, 2, None) == einval  # misaligned workspace
+
+
 def test_last_error_string_starts_empty():
     assert wd.wd_last_error_string() == "none"
 
