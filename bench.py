@@ -214,8 +214,9 @@ def upload_layer(torch, dev, wl, layer):
 class Stack:
     """48 layers of device-resident MXFP8 weights plus per-B routing and buffers."""
 
-    def __init__(self, torch, wd, dev, layers, max_batch, log):
+    def __init__(self, torch, wd, dev, layers, max_batch, log, route="uniform"):
         self.torch, self.wd, self.dev = torch, wd, dev
+        self.route = route
         wl = WORKLOAD
         self.H, self.I, self.E, self.K = wl.H, wl.I, wl.E, wl.K
         self.L = layers
@@ -240,7 +241,7 @@ class Stack:
         wl = WORKLOAD
         ids, ws = [], []
         for l in range(self.L):
-            i, w = synth.route(wl.seed, l, B, self.E, self.K)
+            i, w = synth.route(wl.seed, l, B, self.E, self.K, mode=self.route)
             ids.append(i)
             ws.append(w)
         return np.stack(ids), np.stack(ws)
@@ -733,6 +734,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (profiling runs)")
     ap.add_argument("--batch", type=int, default=HEADLINE_B,
                     help="batch of the headline step (profiling runs; the bench value is B=32)")
+    ap.add_argument("--route", default="uniform", choices=["uniform", "zipf", "fixed", "disjoint"],
+                    help="routing of the stack (profiling runs of the routing-stress layers)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -778,7 +781,7 @@ def main():
     sweep = [int(b) for b in args.sweep.split(",") if b] if not args.quick else []
     extras_on = not args.quick and not args.no_extras
     max_b = max([HEADLINE_B, args.batch] + sweep + (list(CROSSOVER_B) if extras_on else []))
-    stack = Stack(torch, wd, dev, args.layers, max_b, log)
+    stack = Stack(torch, wd, dev, args.layers, max_b, log, route=args.route)
     H, I, E, K = stack.H, stack.I, stack.E, stack.K
 
     def stack_row(B, ms, nb, plan_name=None):
@@ -926,7 +929,7 @@ def main():
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
             "context": {"pages_b200": "3.95 TB/s at B=32 = 58% of a 6.8 TB/s copy peak (B200)"}}
-    if args.quick or args.layers != WORKLOAD.layers or B != HEADLINE_B:
+    if args.quick or args.layers != WORKLOAD.layers or B != HEADLINE_B or args.route != "uniform":
         line["note"] = "profiling run: not a bench value"
     if rank == 0:
         print(json.dumps(line), flush=True)
