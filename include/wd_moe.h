@@ -66,10 +66,9 @@
  * Expert ids are range-checked on the device: an id outside [0, E) contributes
  * nothing (its h entries are written as 0) and sets bit 0 of the workspace
  * error flag, which stays set until wd_moe_read_error_flag reads and clears
- * it.  Duplicate ids within a token are allowed; their contributions add (in
- * the shared-row down kernel two slots of one token on one expert are added
- * by shared-memory atomics, so their order, and the last bit of that output,
- * may differ from run to run; every other result is bit-reproducible).
+ * it.  Duplicate ids within a token are allowed; their contributions add.
+ * No kernel reduces through atomics: every result is bit-reproducible from
+ * run to run.
  *
  * Every entry point that launches work is asynchronous on `stream`: it never
  * synchronises, never allocates, and returns after the launches.  Launch
