@@ -60,7 +60,7 @@ HEADLINE_B = 32
 SWEEP_B = (1, 2, 4, 8, 16, 32)
 # plans timed beside the built-in one on the stack (B >= 8, where they differ)
 COMPARE_PLANS = {
-    "pages_form": "gu=batched:2:1,dn=4:1",   # the pages' two kernels at every B
+    "pages_form": "gu=batched:1:1,dn=4:1",   # the pages' two kernels at every B
     "per_token_down": "gu=mma,dn=4:1,pdl=1",  # shared-row gate/up, per-(token, dims) down
 }
 L2_FLUSH_BYTES = 512 << 20  # written before every cold single-layer call (L2 is 126 MB)

@@ -22,8 +22,10 @@
 
 namespace wd {
 
+// One neuron per warp and one block per lane per pass fits in 64 registers:
+// 4 CTAs (32 warps) per SM, so the B = 1..4 grids need fewer waves.
 template <int NPW, int CPL>
-__global__ void __launch_bounds__(256, 2) moe_gate_up_3d_batched(
+__global__ void __launch_bounds__(256, (NPW == 1 && CPL == 1) ? 4 : 2) moe_gate_up_3d_batched(
     const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const uint8_t* __restrict__ gate_up, const uint8_t* __restrict__ gate_up_scale,
     __nv_bfloat16* __restrict__ h, uint32_t* __restrict__ error_flag, int B, int H, int I,

@@ -174,9 +174,9 @@ def test_built_in_plan_by_batch():
     assert wd.wd_moe_describe_plan(1, **q) == \
         "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<1,6> pdl=3 launches=2"
     assert wd.wd_moe_describe_plan(2, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<2,3> pdl=3 launches=2"
+        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<2,3> pdl=3 launches=2"
     assert wd.wd_moe_describe_plan(4, **q) == \
-        "gate_up=moe_gate_up_3d_batched<2,1> down=moe_down_3d_batched<4,1> pdl=3 launches=2"
+        "gate_up=moe_gate_up_3d_batched<1,1> down=moe_down_3d_batched<4,1> pdl=3 launches=2"
     # tokens share experts: tensor-core gate/up; from B*K >= E on, each routed
     # down row is read once for all of its pairs
     assert wd.wd_moe_describe_plan(8, **q) == \
