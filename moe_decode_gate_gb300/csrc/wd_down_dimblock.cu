@@ -42,11 +42,11 @@
 //   - NS step groups of G consumer warps; group q takes the steps q, q + NS,
 //     ... and owns the S / NS stages they use; each warp of a group does its
 //     part of I (built-in at I = 768: 4 groups of 2 warps with 12 blocks each,
-//     3 stages per group, up to 8 pairs per step).  Before waiting for its
-//     stage, each lane requests its B fragments from global memory: the FP16
-//     h row of its pair (L2-resident, written by moe_h_encode), 16 bytes per
-//     block, so that the h latency overlaps the weights' and h takes no room
-//     in the ring.  Per 32-column block: two k16 MMAs (E4M3 -> FP16 straight
+//     3 stages per group, up to 8 pairs per step).  Each lane requests its B
+//     fragments from global memory one step of its group ahead (two register
+//     buffers): the FP16 h row of its pair (L2-resident, written by
+//     moe_h_encode), 16 bytes per block, so that the h latency overlaps the
+//     previous step and h takes no room in the ring.  Per 32-column block: two k16 MMAs (E4M3 -> FP16 straight
 //     into the A fragments, exact) from a zero tile, then the tile times the
 //     rows' power-of-two block scales (decoded through a 256-entry table)
 //     into FP32 sums;
@@ -305,13 +305,13 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
   const uint32_t a_base = (uint32_t)(j0 * 512);  // slab of the first block
   const uint32_t s_off = (uint32_t)(kDRows * I + pg * nblk + j0);
   bool dead = false;
-  for (int i = grp; i < nsteps; i += NS) {
+  // B fragments of step i: this lane's columns of pair g's FP16 h row, 8
+  // values (16 bytes) per block, straight from global memory (written by the
+  // kernel before this one, resident in L2).  They are requested one step of
+  // the group ahead (two register buffers), so the L2 latency overlaps the
+  // previous step's wait and MMAs.  Columns >= pairs stay zero.
+  auto load_b = [&](int i, uint4 (&bf)[NB]) {
     const int4 st_info = step_tab[step_at(i)];
-    // B fragments: this lane's columns of pair g's FP16 h row, 8 values (16
-    // bytes) per block, straight from global memory (written by the kernel
-    // before this one, resident in L2); requested before waiting for the
-    // weights so that both latencies overlap.  Columns >= pairs stay zero.
-    uint4 bf[NB];
     const int slot_g = g < st_info.z ? rt.slots[st_info.y + g] : -1;
     if (slot_g >= 0) {
       const uint8_t* hrow = hg + (size_t)slot_g * I * 2 + (size_t)(j0 * 64 + tig * 16);
@@ -321,12 +321,27 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
 #pragma unroll
       for (int m = 0; m < NB; ++m) bf[m] = make_uint4(0u, 0u, 0u, 0u);
     }
-    const uint32_t s = i % S;
+  };
+  // step i of the group uses stage s with phase parity ph (kept incrementally:
+  // the group's steps advance the stage by NS, a divisor of S)
+  uint32_t s_cur = (uint32_t)grp, ph_cur = 0;
+  auto step = [&](int i, const uint4 (&bf)[NB]) {
+    const int4 st_info = step_tab[step_at(i)];
+    const uint32_t s = s_cur, ph = ph_cur;
+    s_cur += NS;
+    if (s_cur >= (uint32_t)S) {
+      s_cur -= S;
+      ph_cur ^= 1u;
+    }
+    // the result rows of this lane's two pair columns, looked up before the wait
+    const int pc0 = 2 * tig;
+    float* r0 = pc0 < st_info.z ? res + rt.slots[st_info.y + pc0] * kDRows : nullptr;
+    float* r1 = pc0 + 1 < st_info.z ? res + rt.slots[st_info.y + pc0 + 1] * kDRows : nullptr;
     bool ok;
-    const uint32_t tok = mbar_wait_token(full + 8 * s, (i / S) & 1, ok);
+    const uint32_t tok = mbar_wait_token(full + 8 * s, ph, ok);
     if (!ok) {
       dead = true;
-      break;
+      return;
     }
     const uint32_t st = ring + s * L.stage + tok;
     // two accumulators (even and odd blocks) halve the scale-FMA chain
@@ -355,15 +370,23 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
     __syncwarp();
     if (lane == 0) mbar_arrive_after(empty + 8 * s, acc);
     // this lane's pair columns 2 tig, 2 tig + 1: its part's sums of those slots
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int pc = 2 * tig + q;
-      if (pc < st_info.z) {
-        float* r = res + rt.slots[st_info.y + pc] * kDRows;
-        r[pg] = acc[0][q] + acc[1][q];
-        r[pg + 8] = acc[0][2 + q] + acc[1][2 + q];
-      }
+    if (r0) {
+      r0[pg] = acc[0][0] + acc[1][0];
+      r0[pg + 8] = acc[0][2] + acc[1][2];
     }
+    if (r1) {
+      r1[pg] = acc[0][1] + acc[1][1];
+      r1[pg + 8] = acc[0][3] + acc[1][3];
+    }
+  };
+  uint4 bfa[NB], bfb[NB];
+  if (grp < nsteps) load_b(grp, bfa);
+  for (int i = grp; i < nsteps && !dead; i += 2 * NS) {
+    if (i + NS < nsteps) load_b(i + NS, bfb);
+    step(i, bfa);
+    if (i + NS >= nsteps || dead) break;
+    if (i + 2 * NS < nsteps) load_b(i + 2 * NS, bfa);
+    step(i + NS, bfb);
   }
   if (dead && lane == 0 && error_flag) atomicOr(error_flag, 2u);
   // all slots' results are in: y = sum over k of result * w * 2^-k, k in order
