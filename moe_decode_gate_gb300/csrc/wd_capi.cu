@@ -48,7 +48,7 @@ bool parse_plan(const char* spec, PlanOverride* out) {
     char* save = nullptr;
     for (char* tok = strtok_r(buf, ",", &save); tok; tok = strtok_r(nullptr, ",", &save)) {
       int a = 0, b = 0;
-      if (sscanf(tok, "gu=batched:%d:%d", &a, &b) == 2) {
+      if (int n = 0; sscanf(tok, "gu=batched:%d:%d%n", &a, &b, &n) == 2 && tok[n] == 0) {
         p.gu_variant = kGateUpBatched;
         p.gu_npw = a;
         p.gu_cpl = b;

@@ -216,6 +216,8 @@ def test_plan_override_parser():
     lib = wd.lib()
     assert lib.wd_moe_set_plan(b"gu=rowshare:2:1,dn=4:1,rowshare_min_b=4") == OK
     assert lib.wd_moe_set_plan(b"gu=batched:2:1") == OK
+    assert lib.wd_moe_set_plan(b"gu=batched:2:1x") == INVALID
+    assert lib.wd_moe_set_plan(b"gu=batched:1:1:2") == INVALID
     assert lib.wd_moe_set_plan(b"gu=persist:2:2,dn=4:1") == OK
     assert lib.wd_moe_set_plan(b"gu=mma,pdl=3") == OK
     assert lib.wd_moe_set_plan(b"gu=mma:2,pdl=0") == OK
