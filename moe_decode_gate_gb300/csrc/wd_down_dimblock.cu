@@ -90,7 +90,7 @@ __host__ __device__ constexpr int d_round(int v, int a) { return (v + a - 1) / a
 // results [G][B*K][16] FP32 (one table per part of I when G warps share a
 // step).
 struct DimLayout {
-  int stage, bars, dec, steps, res, ring, total;
+  int stage, bars, dec, steps, res, fold, ring, total;
 };
 
 __host__ __device__ inline DimLayout dim_layout(int I, int S, int G) {
@@ -100,7 +100,8 @@ __host__ __device__ inline DimLayout dim_layout(int I, int S, int G) {
   L.dec = L.bars + 16 * kDMaxStages;
   L.steps = L.dec + 256 * 4;
   L.res = L.steps + kDMaxSteps * 16;
-  L.ring = d_round(L.res + G * kStreamMaxSlots * kDRows * 4, 1024);
+  L.fold = L.res + G * kStreamMaxSlots * kDRows * 4;  // per slot: w * 2^-k split in two factors
+  L.ring = d_round(L.fold + kStreamMaxSlots * 8, 1024);
   L.total = L.ring + S * L.stage;
   return L;
 }
@@ -290,6 +291,18 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
   // and the writes of `out` below must follow it too
   const uint32_t wait_token = grid_dependency_wait();
   const uint8_t* hg = reinterpret_cast<const uint8_t*>(h16) + wait_token;
+  // each slot's factors for the final fold, w * 2^-(k >> 1) and 2^-(k - (k >> 1)),
+  // fetched now so that their latency hides behind the steps (0 for bad ids)
+  float2* fold = reinterpret_cast<float2*>(smem + L.fold);
+  for (int j = tid; j < BK; j += NW * 32) {
+    const int e = rt.ids[j];
+    float2 f = make_float2(0.0f, 0.0f);
+    if (e >= 0 && e < E) {
+      const int ke = __ldcg(hk + j + wait_token);
+      f = make_float2(__ldg(topk_w + j) * exp2_int(-(ke >> 1)), exp2_int(-(ke - (ke >> 1))));
+    }
+    fold[j] = f;
+  }
   const int g = lane >> 2, tig = lane & 3;
   const int pg = slab_row(g);  // the output dim (of 16) of tile rows g and g + 8
   const int grp = warp % NS, part = warp / NS;
@@ -399,11 +412,10 @@ __global__ void __launch_bounds__(32 * (kDMaxWarps + kDProducers), 1) moe_down_d
       const int slot = b * K + k;
       const int e = rt.ids[slot];
       if (e < 0 || e >= E) continue;
-      const int ke = __ldcg(hk + slot + wait_token);
-      const float f1 = exp2_int(-(ke >> 1)), f2 = exp2_int(-(ke - (ke >> 1)));
+      const float2 f = fold[slot];
       float r = res[slot * kDRows + row];
       for (int h = 1; h < G; ++h) r += res[(h * BK + slot) * kDRows + row];
-      y = fmaf((r * f1) * f2, __ldg(topk_w + slot), y);
+      y = fmaf(r * f.y, f.x, y);
     }
     out[(size_t)b * H + d0 + row] = __float2bfloat16_rn(y);
   }
