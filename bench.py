@@ -40,6 +40,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -120,20 +121,57 @@ def kernel_sources_sha():
     return h.hexdigest()[:16]
 
 
+# The translation unit that defines each layer kernel.
+KERNEL_SOURCE = {
+    "moe_gate_up_3d_batched": "wd_gate_up.cu",
+    "moe_down_3d_batched": "wd_down.cu",
+    "moe_gate_up_mma": "wd_gate_up_mma.cu",
+    "moe_down_dimblock": "wd_down_dimblock.cu",
+    "moe_h_encode": "wd_down_dimblock.cu",
+    "moe_gate_up_persist": "wd_gate_up_persist.cu",
+    "moe_gate_up_rowshare": "wd_gate_up_rowshare.cu",
+}
+
+
+def kernel_file_sha(kernel):
+    """sha256 prefix of the file that defines `kernel` and of every csrc header
+    it includes, directly or through another header; None for an unknown
+    kernel.  A DRAM count taken on one kernel stays valid while these files are
+    unchanged, whatever happens to the other kernels' files."""
+    csrc = os.path.join(ROOT, "moe_decode_gate_gb300", "csrc")
+    top = KERNEL_SOURCE.get(kernel)
+    if top is None:
+        return None
+    seen, todo = set(), [top]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo += re.findall(r'^#include "([^"/]+)"', fh.read(), re.M)
+    h = hashlib.sha256()
+    for f in sorted(seen):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel, mean_alg_bytes):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources, scaled from the profiled launch to a launch
-    with the mean algorithmic bytes (dram / algorithmic of the SAME profiled
-    launch, times the mean); else None."""
+    the kernel's current sources (its own file and the headers it includes),
+    scaled from the profiled launch to a launch with the mean algorithmic
+    bytes (dram / algorithmic of the SAME profiled launch, times the mean);
+    else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("sources_sha") != kernel_sources_sha():
-        return None
     k = d.get("kernels", {}).get(kernel)
     if not k or not k.get("algorithmic_bytes_profiled_launch"):
+        return None
+    if k.get("kernel_sources_sha") != kernel_file_sha(kernel):
         return None
     ratio = k["dram_bytes_profiled_launch"] / k["algorithmic_bytes_profiled_launch"]
     return {"bytes_per_launch": round(ratio * mean_alg_bytes), "dram_over_algorithmic": round(ratio, 4),
@@ -905,7 +943,8 @@ def main():
         torch.cuda.empty_cache()
         extras["single_layers_cold"] = {
             "what": "one layer of each single-layer workload as a CUDA graph replay, L2 flushed "
-                    "(512 MB written, untimed) before every timed replay, median of 20 replays",
+                    "(512 MB written, then read, untimed) before every timed replay, median of "
+                    "20 replays",
             "rows": time_single_layers(torch, wd, dev, peak_ref, 20, log)}
 
     # ---- CPU oracle on a bounded sample (rank 0) ----

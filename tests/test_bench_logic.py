@@ -42,19 +42,34 @@ def test_roofline_names_the_kernel_with_the_longest_launch():
 def test_traffic_comes_from_the_same_profiled_launch_and_only_for_current_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
-    data = {"sources_sha": bench.kernel_sources_sha(),
-            "kernels": {"moe_k": {"dram_bytes_profiled_launch": 1010, "algorithmic_bytes_profiled_launch": 1000,
-                                  "profiled": "x"}}}
+    data = {"kernels": {"moe_k": {"dram_bytes_profiled_launch": 1010, "algorithmic_bytes_profiled_launch": 1000,
+                                  "profiled": "x", "kernel_sources_sha": "1111222233334444"}}}
     (prof / "dram_traffic.json").write_text(json.dumps(data))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    current = data["sources_sha"]
-    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: current)
+    monkeypatch.setattr(bench, "kernel_file_sha", lambda k: "1111222233334444")
     t = bench.profile_traffic("moe_k", 2000)
     assert t["bytes_per_launch"] == 2020 and t["dram_over_algorithmic"] == 1.01
     assert bench.profile_traffic("other", 2000) is None
-    data["sources_sha"] = "0000000000000000"  # sources changed since the capture
+    data["kernels"]["moe_k"]["kernel_sources_sha"] = "0000000000000000"  # kernel changed since the capture
     (prof / "dram_traffic.json").write_text(json.dumps(data))
     assert bench.profile_traffic("moe_k", 2000) is None
+
+
+def test_kernel_file_hash_follows_the_kernels_own_file_and_its_headers(tmp_path, monkeypatch):
+    csrc = tmp_path / "moe_decode_gate_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cuh").write_text("// shared\n")
+    (csrc / "b.cuh").write_text('#include "a.cuh"\n')
+    (csrc / "k1.cu").write_text('#include "b.cuh"\n__global__ void k1() {}\n')
+    (csrc / "k2.cu").write_text('#include "a.cuh"\n__global__ void k2() {}\n')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCE", {"k1": "k1.cu", "k2": "k2.cu"})
+    h1, h2 = bench.kernel_file_sha("k1"), bench.kernel_file_sha("k2")
+    (csrc / "k2.cu").write_text('#include "a.cuh"\n__global__ void k2() { }\n')
+    assert bench.kernel_file_sha("k1") == h1 and bench.kernel_file_sha("k2") != h2
+    (csrc / "a.cuh").write_text("// shared, edited\n")  # reached from k1 through b.cuh
+    assert bench.kernel_file_sha("k1") != h1
+    assert bench.kernel_file_sha("unknown") is None
 
 
 def test_committed_traffic_profile_has_both_figures_for_every_plan_kernel():
