@@ -2,6 +2,7 @@
 algorithmic bytes per launch, the roofline's choice of kernel, and the DRAM
 traffic taken from the committed profile only while it matches the sources."""
 import json
+import re
 import os
 
 import numpy as np
@@ -80,3 +81,11 @@ def test_committed_traffic_profile_has_both_figures_for_every_plan_kernel():
         k = d["kernels"][name]
         ratio = k["dram_bytes_profiled_launch"] / k["algorithmic_bytes_profiled_launch"]
         assert 0.95 < ratio < 1.1, (name, ratio)  # each routed row read from HBM once
+
+
+def test_kernel_source_map_names_the_file_that_defines_each_kernel():
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "moe_decode_gate_gb300", "csrc")
+    for kernel, f in bench.KERNEL_SOURCE.items():
+        text = open(os.path.join(csrc, f)).read()
+        assert re.search(r"__global__[^;{]*\b" + kernel + r"\s*\(", text), (kernel, f)
