@@ -82,6 +82,19 @@ def test_expert_centric_layer_matches_its_definition(cuda_device, B, H, I, E, K,
             f"expert-centric B={B} H={H} I={I} {route}")
 
 
+# The largest batch of the crossover sweep on the full-size layer: the GPU
+# runs all 256 tokens, the definition is assembled for a seeded sample (each
+# token's output depends only on its own row, ids and weights).
+def test_expert_centric_crossover_batch_on_sampled_tokens(cuda_device):
+    B, H, I, E, K = 256, 2048, 768, 128, 8
+    xs, ids, w, gu, gus, dn, dns = _case(900, B, H, I, E, K)
+    got = run_expert_centric(cuda_device, xs, ids, w, gu, gus, dn, dns)
+    pick = np.sort(np.random.default_rng(B).choice(B, 8, replace=False))
+    want = expert_centric_expected(np.ascontiguousarray(xs[pick]), np.ascontiguousarray(ids[pick]),
+                                   np.ascontiguousarray(w[pick]), gu, gus, dn, dns, I, E)
+    compare(got[pick], want, f"expert-centric B={B} sampled tokens {pick.tolist()}")
+
+
 def test_expert_centric_skips_bad_ids(cuda_device):
     xs, ids, w, gu, gus, dn, dns = _case(41, 4, 256, 128, 8, 3)
     ids = ids.copy()

@@ -77,6 +77,26 @@ def test_qwen3_routing_stress_b32(cuda_device, name):
     check_layer(cuda_device, *inputs(wl, 32), *weights(wl), name)
 
 
+# The batches of the crossover sweep, beyond decode (B = 128 and 256 on the
+# full-size layer, the built-in plan the bench times there): the GPU runs every
+# token, the oracle a seeded sample of them.  A token's h rows and output
+# depend only on its own x row, ids and weights, so the sampled rows are
+# compared element by element.
+@pytest.mark.parametrize("B", [128, 256])
+def test_crossover_batches_on_sampled_tokens(cuda_device, B):
+    wl = synth.WORKLOADS["qwen3_sweep"]
+    xs, ids, w = inputs(wl, B)
+    gu, gus, dn, dns = weights(wl)
+    got, got_h, flag = run_layer(cuda_device, xs, ids, w, gu, gus, dn, dns)
+    pick = np.sort(np.random.default_rng(B).choice(B, 12, replace=False))
+    want, want_h, _, bad = oracle.moe_decode(xs[pick], ids[pick], w[pick], gu, gus, dn, dns,
+                                             wl.I, wl.E, with_f64=True)
+    what = f"B={B} sampled tokens {pick.tolist()} ({wd.wd_moe_describe_plan(B, wl.H, wl.I, wl.E, wl.K)})"
+    compare(got_h[pick].reshape(-1, wl.I), want_h.reshape(-1, wl.I), what + " h")
+    compare(got[pick], want, what + " out")
+    assert flag == 0 and bad == 0
+
+
 def test_gate_up_kernel_alone(cuda_device):
     wl = synth.WORKLOADS["qwen3_b1"]
     gu, gus, _, _ = weights(wl)
