@@ -67,13 +67,19 @@ __device__ __forceinline__ int routed_index(const RoutingTables& t, int e) {
 
 // Build the tables with all `nthreads` threads of the CTA (contains
 // __syncthreads; every thread must call it).  `chunk` is the number of slots
-// per chunk (work items split an expert's token list into chunks).
+// per chunk (work items split an expert's token list into chunks).  Every
+// phase but the two short scans is spread over all threads: the lists are
+// filled through shared-memory atomics in any order, then each slot moves to
+// its rank among its list's slots (found through `chunk_u`, which is filled
+// last), so the lists end in ascending slot order whatever the order of the
+// atomics.
 __device__ __forceinline__ void build_routing_tables(const RoutingTables& t,
                                                      const int32_t* __restrict__ ids, int BK,
                                                      int E, int chunk, int nthreads) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwords = (E + 31) >> 5;
   for (int i = tid; i < nwords; i += nthreads) t.mask[i] = 0u;
+  for (int i = tid; i < kStreamMaxSlots; i += nthreads) t.cnt[i] = 0;
   for (int s = tid; s < BK; s += nthreads) t.ids[s] = __ldg(ids + s);  // the only global reads
   if (tid == 0) t.scalar[2] = 0;
   __syncthreads();
@@ -85,31 +91,28 @@ __device__ __forceinline__ void build_routing_tables(const RoutingTables& t,
       t.scalar[2] = 1;
   }
   __syncthreads();
+  // routed experts before each mask word
   if (warp == 0) {
     int base = 0;
     for (int w0 = 0; w0 < nwords; w0 += 32) {
       const uint32_t word = (w0 + lane < nwords) ? t.mask[w0 + lane] : 0u;
       int excl, total;
       warp_exclusive_scan(__popc(word), excl, total);
-      if (w0 + lane < nwords) {
-        t.wbase[w0 + lane] = base + excl;
-        uint32_t wd = word;
-        for (int i = base + excl; wd; ++i, wd &= wd - 1u) {
-          t.expert[i] = (w0 + lane) * 32 + (__ffs(wd) - 1);
-          t.cnt[i] = 0;
-        }
-      }
+      if (w0 + lane < nwords) t.wbase[w0 + lane] = base + excl;
       base += total;
     }
     if (lane == 0) t.scalar[0] = base;
   }
   __syncthreads();
-  const int U = t.scalar[0];
+  // the routed experts in ascending order, and each one's slot count
+  for (int e = tid; e < E; e += nthreads)
+    if (t.mask[e >> 5] & (1u << (e & 31))) t.expert[routed_index(t, e)] = e;
   for (int s = tid; s < BK; s += nthreads) {
     const int e = t.ids[s];
     if (e >= 0 && e < E) atomicAdd(&t.cnt[routed_index(t, e)], 1);
   }
   __syncthreads();
+  const int U = t.scalar[0];
   if (warp == 0) {
     int base = 0, cbase = 0;
     for (int u0 = 0; u0 < U; u0 += 32) {
@@ -122,7 +125,6 @@ __device__ __forceinline__ void build_routing_tables(const RoutingTables& t,
       if (u < U) {
         t.off[u] = base + excl;
         t.coff[u] = cbase + cexcl;
-        for (int q = 0; q < nch; ++q) t.chunk_u[cbase + cexcl + q] = u;
         t.cnt[u] = 0;  // becomes the fill cursor
       }
       base += total;
@@ -135,23 +137,39 @@ __device__ __forceinline__ void build_routing_tables(const RoutingTables& t,
     }
   }
   __syncthreads();
-  // fill the lists in ascending slot order: warp 0 walks the slots 32 at a
-  // time; lanes holding the same expert rank themselves with a match mask
-  if (warp == 0) {
-    for (int s0 = 0; s0 < BK; s0 += 32) {
-      const int s = s0 + lane;
-      const int e = (s < BK) ? t.ids[s] : -1;
-      const bool valid = e >= 0 && e < E;
-      const unsigned same = __match_any_sync(0xFFFFFFFFu, valid ? e : -1 - lane);
-      int u = 0;
-      if (valid) {
-        u = routed_index(t, e);
-        t.slots[t.off[u] + t.cnt[u] + __popc(same & ((1u << lane) - 1u))] = s;
-      }
-      __syncwarp();
-      if (valid && (__ffs(same) - 1) == lane) t.cnt[u] += __popc(same);
-      __syncwarp();
+  // each slot takes a place in its expert's list, in any order ...
+  for (int s = tid; s < BK; s += nthreads) {
+    const int e = t.ids[s];
+    if (e >= 0 && e < E) {
+      const int u = routed_index(t, e);
+      t.slots[t.off[u] + atomicAdd(&t.cnt[u], 1)] = s;
     }
+  }
+  __syncthreads();
+  // ... then its rank in ascending slot order: the list's slots below it
+  for (int s = tid; s < BK; s += nthreads) {
+    const int e = t.ids[s];
+    int pos = -1;
+    if (e >= 0 && e < E) {
+      const int u = routed_index(t, e);
+      const int* l = t.slots + t.off[u];
+      const int n = t.off[u + 1] - t.off[u];
+      int r = 0;
+      for (int i = 0; i < n; ++i) r += l[i] < s;
+      pos = t.off[u] + r;
+    }
+    t.chunk_u[s] = pos;  // scratch: where slot s goes
+  }
+  __syncthreads();
+  for (int s = tid; s < BK; s += nthreads) {
+    const int pos = t.chunk_u[s];
+    if (pos >= 0) t.slots[pos] = s;
+  }
+  __syncthreads();
+  // the chunks of each routed expert's list
+  for (int u = tid; u < U; u += nthreads) {
+    const int nch = (t.off[u + 1] - t.off[u] + chunk - 1) / chunk;
+    for (int q = 0; q < nch; ++q) t.chunk_u[t.coff[u] + q] = u;
   }
   __syncthreads();
 }
